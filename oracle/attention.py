@@ -1,0 +1,225 @@
+"""Exact-attention oracle: plain, slow, fp64, CPU.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module. The product path (``exact_attention_30_gb300``) never imports it and
+shares no code with it: no kernels, helpers, constants or pre/post-processing.
+
+What it computes (all arithmetic in float64, numpy; a BLAS matmul is the only
+library primitive used as a step):
+
+* ``attention_fwd`` -- the plain definition O = softmax(scale * Q K^T) V with
+  S and P materialised, as written in "Lesson 1: FlashAttention core idea" §1
+  and in the naive three-step decomposition of "Interview Q15: FlashAttention"
+  (Step 1-3) and "FlashAttention and Triton" §19.2. The softmax is the
+  max-subtracted one of "FlashAttention and Triton" §19.12
+  (``standard_attention``) and §19.11. It also returns the per-row
+  log-sum-exp LSE = m + ln(l) of the scaled scores: the per-row statistics
+  that "Lesson 1" §5 says are the only thing kept for the backward pass.
+* ``attention_bwd`` -- dQ, dK, dV from the chain rule through the same
+  definition, in the notation of "Lesson 1" §5 (backward by recomputation):
+  dV = P^T dO, dP = dO V^T, dS = P o (dP - rowsum(dP o P)) * scale,
+  dQ = dS K, dK = dS^T Q. The row sum is taken over the whole row of P.
+* ``tiled_attention_fwd`` -- the tiled online-softmax algorithm, step by step
+  as "Lesson 1" §4 and "FlashAttention and Triton" §19.12 (``tiled_attention``)
+  describe it: query tiles outer, key/value tiles inner, running max m,
+  running denominator l and unnormalised accumulator rescaled by exp(m - m_new).
+  Used only to check the oracle against itself (the pages claim the two agree
+  to < 1e-12), never as the reference for the GPU path.
+* ``online_softmax_stats`` -- the (m, l) recurrence of "Lesson 1" §3 over a
+  list of score blocks, for the worked example of "FlashAttention and Triton"
+  §19.5 (scores [1, 2] then [3, 4]).
+
+Readings where the pages are silent (each also listed in the design notes):
+* ``scale`` is a free argument; the pages fix 1/sqrt(d). dS carries exactly one
+  factor of ``scale`` (the pages' "/ sqrt(d)" in the dS line).
+* LSE is the natural-log log-sum-exp of the *scaled* scores.
+* Inputs are taken exactly as given (bf16 or fp32 values upcast exactly to
+  fp64); outputs are fp64.
+
+Pins (tests/test_oracle_pins.py): the worked example, the mini-lab agreement
+of naive and tiled paths, row-stochastic P, closed forms (N = 1, Q = 0, a
+dominant key, permutation and key-shift invariance), PyTorch's float64 CPU
+scaled_dot_product_attention + autograd, and central finite differences for
+the backward pass. No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "scores",
+    "row_softmax",
+    "attention_fwd",
+    "attention_bwd",
+    "attention_fwd_rows",
+    "tiled_attention_fwd",
+    "online_softmax_stats",
+    "attention_fwd_batched",
+    "attention_bwd_batched",
+]
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def scores(Q, K, scale: float) -> np.ndarray:
+    """S = scale * Q K^T, materialised (N_q x N_k).
+
+    "Lesson 1: FlashAttention core idea" §1 (the formula and the explicit
+    intermediate matrices); "Interview Q15" Step 1.
+    """
+    return float(scale) * (_f64(Q) @ _f64(K).T)
+
+
+def row_softmax(S):
+    """Numerically stable row softmax: returns (P, m, l).
+
+    m_r = max_c S_rc, E = exp(S - m_r), l_r = sum_c E_rc, P = E / l_r.
+    "FlashAttention and Triton" §19.12 (``standard_attention``) and §19.11
+    (subtract the row max, exponentiate, sum, divide).
+    """
+    S = _f64(S)
+    m = S.max(axis=1)
+    E = np.exp(S - m[:, None])
+    l = E.sum(axis=1)
+    P = E / l[:, None]
+    return P, m, l
+
+
+def attention_fwd(Q, K, V, scale: float):
+    """Exact attention forward for one head: (O, LSE).
+
+    O = softmax(scale * Q K^T) V ("Lesson 1" §1; "Interview Q15" Steps 1-3;
+    "FlashAttention and Triton" §19.2). LSE_r = m_r + ln(l_r): the per-row
+    statistics that "Lesson 1" §5 keeps for the backward pass, folded into one
+    number.
+    Q: [N_q, d], K: [N_k, d], V: [N_k, d_v].
+    """
+    S = scores(Q, K, scale)
+    P, m, l = row_softmax(S)
+    O = P @ _f64(V)
+    LSE = m + np.log(l)
+    return O, LSE
+
+
+def attention_fwd_rows(Q, K, V, scale: float, rows):
+    """The definition of ``attention_fwd`` evaluated for the query rows ``rows`` only.
+
+    Softmax is row-local ("FlashAttention and Triton" §19.11: one program per
+    row), so row r of O and LSE depends only on query row r and all of K, V.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    return attention_fwd(_f64(Q)[rows], K, V, scale)
+
+
+def attention_bwd(Q, K, V, dO, scale: float):
+    """Exact attention backward for one head: (dQ, dK, dV).
+
+    "Lesson 1: FlashAttention core idea" §5, written for whole matrices:
+      S  = scale * Q K^T,  P = softmax(S)   (rows)
+      dV = P^T dO
+      dP = dO V^T
+      dS = P o (dP - rowsum(dP o P)) * scale
+      dQ = dS K
+      dK = dS^T Q
+    The row sum runs over the full row (the page shows it inside a per-tile
+    loop; only the full-row sum is the gradient of softmax).
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    S = scores(Q, K, scale)
+    P, _, _ = row_softmax(S)
+    dV = P.T @ dO
+    dP = dO @ V.T
+    D = (dP * P).sum(axis=1)
+    dS = P * (dP - D[:, None]) * float(scale)
+    dQ = dS @ K
+    dK = dS.T @ Q
+    return dQ, dK, dV
+
+
+def tiled_attention_fwd(Q, K, V, scale: float, q_tile: int = 4, k_tile: int = 4):
+    """Tiled forward with online softmax (self-check of the oracle only).
+
+    The algorithm of "Lesson 1" §4 (query tiles outer, key/value tiles inner)
+    as run by the CPU simulator of "FlashAttention and Triton" §19.12: per
+    query tile keep a running max m (start -inf), a running denominator l
+    (start 0) and an unnormalised accumulator acc (start 0); for each key tile
+    form the local scores s, m_new = max(m, rowmax(s)), alpha = exp(m - m_new),
+    p = exp(s - m_new), l = l * alpha + rowsum(p), acc = acc * alpha + p V_j,
+    m = m_new; after the last key tile divide acc by l. Ragged last tiles are
+    whatever remains (the pages' ceil(N / B)).
+    Returns (O, LSE) with LSE = m + ln(l).
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    n_q, n_k, d_v = Q.shape[0], K.shape[0], V.shape[1]
+    O = np.zeros((n_q, d_v))
+    LSE = np.zeros(n_q)
+    for q0 in range(0, n_q, q_tile):
+        q = Q[q0:q0 + q_tile]
+        m = np.full(q.shape[0], -np.inf)
+        l = np.zeros(q.shape[0])
+        acc = np.zeros((q.shape[0], d_v))
+        for k0 in range(0, n_k, k_tile):
+            s = float(scale) * (q @ K[k0:k0 + k_tile].T)
+            m_new = np.maximum(m, s.max(axis=1))
+            alpha = np.exp(m - m_new)  # exp(-inf) = 0 on the first tile
+            p = np.exp(s - m_new[:, None])
+            l = l * alpha + p.sum(axis=1)
+            acc = acc * alpha[:, None] + p @ V[k0:k0 + k_tile]
+            m = m_new
+        O[q0:q0 + q_tile] = acc / l[:, None]
+        LSE[q0:q0 + q_tile] = m + np.log(l)
+    return O, LSE
+
+
+def online_softmax_stats(blocks):
+    """Running (m, l) after each block of one score row.
+
+    "Lesson 1" §3: m_new = max(m, m_tile);
+    l_new = l * exp(m - m_new) + l_tile * exp(m_tile - m_new), where
+    l_tile = sum(exp(block - m_tile)). Starts from m = -inf, l = 0.
+    Returns a list of (m, l) pairs, one per block.
+    """
+    m, l = -np.inf, 0.0
+    out = []
+    for blk in blocks:
+        blk = _f64(blk)
+        m_tile = blk.max()
+        l_tile = np.exp(blk - m_tile).sum()
+        m_new = max(m, m_tile)
+        l = l * np.exp(m - m_new) + l_tile * np.exp(m_tile - m_new)
+        m = m_new
+        out.append((float(m), float(l)))
+    return out
+
+
+def attention_fwd_batched(Q, K, V, scale: float, heads=None):
+    """``attention_fwd`` applied to every (b, h) of [B, H, N, d] arrays.
+
+    ``heads``: optional list of (b, h) pairs to compute; others stay NaN.
+    Returns O [B, H, N, d_v] and LSE [B, H, N] (float64).
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, H, N = Q.shape[:3]
+    O = np.full((B, H, N, V.shape[-1]), np.nan)
+    LSE = np.full((B, H, N), np.nan)
+    for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
+        O[b, h], LSE[b, h] = attention_fwd(Q[b, h], K[b, h], V[b, h], scale)
+    return O, LSE
+
+
+def attention_bwd_batched(Q, K, V, dO, scale: float, heads=None):
+    """``attention_bwd`` applied to every (b, h) of [B, H, N, d] arrays.
+
+    ``heads``: optional list of (b, h) pairs to compute; others stay NaN.
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H = Q.shape[:2]
+    dQ = np.full(Q.shape, np.nan)
+    dK = np.full(K.shape, np.nan)
+    dV = np.full(V.shape, np.nan)
+    for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
+        dQ[b, h], dK[b, h], dV[b, h] = attention_bwd(Q[b, h], K[b, h], V[b, h], dO[b, h], scale)
+    return dQ, dK, dV
