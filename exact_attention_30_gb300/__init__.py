@@ -1,0 +1,186 @@
+"""exact_attention_30_gb300 -- fused exact attention for GB300 (sm_103a).
+
+A thin Python binding over the C ABI in ``include/fa.h`` (``libfa_gb300.so``).
+It only marshals arguments: checks that tensors live on the GPU, are
+contiguous and of the right dtype, allocates outputs with PyTorch (device
+memory is PyTorch's job here) and passes raw pointers plus the current CUDA
+stream to the library. Every step of the computation runs in the library's
+CUDA kernels; there is no CPU path. If the shared library has not been built
+(``python -m exact_attention_30_gb300.build``), every call raises.
+
+    o, lse = fa_fwd(q, k, v, scale)                 # q,k,v: [B,H,N,d] cuda
+    dq, dk, dv = fa_bwd(q, k, v, o, do, lse, scale)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+__all__ = [
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_check_device_status",
+    "fa_debug_timeout_probe", "fa_status_string", "fa_version", "library_path", "load_library",
+    "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
+    "FA_F32", "FA_BF16", "FAError",
+]
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_F32, FA_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+_lib = None
+
+_vp, _ci, _cf, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGNATURES = {
+    "fa_fwd": (_ci, [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_bwd_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
+    "fa_bwd": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_check_device_status": (_ci, [_vp]),
+    "fa_debug_timeout_probe": (_ci, [ctypes.c_longlong, _vp]),
+    "fa_status_string": (ctypes.c_char_p, [_ci]),
+    "fa_version": (_ci, []),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {fa_status_string(code)}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load ``libfa_gb300.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"{_LIB_PATH} is missing: build it with `python -m exact_attention_30_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def header_functions(header_path: str | None = None):
+    """Names of the functions declared in include/fa.h (for export checks)."""
+    path = header_path or os.path.join(os.path.dirname(_HERE), "include", "fa.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def fa_status_string(code: int) -> str:
+    return load_library().fa_status_string(int(code)).decode()
+
+
+def fa_version() -> int:
+    return load_library().fa_version()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float32:
+        return FA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.bfloat16 or torch.float32")
+
+
+def _check(t: torch.Tensor, name: str, like: torch.Tensor | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (this library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B,H,N,d]")
+    if like is not None and (t.shape != like.shape or t.dtype != like.dtype or t.device != like.device):
+        raise ValueError(f"{name} must match q in shape, dtype and device")
+
+
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _raise(code: int, where: str):
+    if code != FA_OK:
+        raise FAError(code, where)
+
+
+def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None):
+    """Forward pass: returns (O [B,H,N,d] like q, LSE [B,H,N] float32)."""
+    lib = load_library()
+    _check(q, "q")
+    _check(k, "k", q)
+    _check(v, "v", q)
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, d]")
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "out", q)
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_cuda:
+        raise ValueError("lse must be float32 [B,H,N] on the same device")
+    with torch.cuda.device(q.device):
+        rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, N, d, scale, _dtype_code(q), _stream_ptr(q.device))
+    _raise(rc, "fa_fwd")
+    return o, lse
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int, dtype=torch.bfloat16) -> int:
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F32
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N, d, code))
+
+
+def fa_bwd(q, k, v, o, do, lse, scale: float | None = None, workspace=None, dq=None, dk=None,
+           dv=None):
+    """Backward pass: returns (dQ, dK, dV), each like q."""
+    lib = load_library()
+    _check(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check(t, n, q)
+    B, H, N, d = q.shape
+    if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B,H,N] on the same device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    ws_bytes = fa_bwd_workspace_bytes(B, H, N, d, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n, q)
+    with torch.cuda.device(q.device):
+        rc = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                        workspace.data_ptr(), workspace.numel(), B, H, N, d, scale,
+                        _dtype_code(q), _stream_ptr(q.device))
+    _raise(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_check_device_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status code."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(load_library().fa_check_device_status(_stream_ptr(dev)))
+
+
+def fa_debug_timeout_probe(limit_ns: int, device=None) -> int:
+    """Launch the bounded-wait probe kernel (see include/fa.h); returns the launch status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(load_library().fa_debug_timeout_probe(int(limit_ns), _stream_ptr(dev)))

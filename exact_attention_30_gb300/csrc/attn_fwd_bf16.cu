@@ -1,0 +1,369 @@
+// attn_fwd_bf16.cu -- fused exact-attention forward on sm_103a tensor cores.
+//
+// What it computes ("Lesson 1: FlashAttention core idea" §4, query tiles
+// outer / key-value tiles inner; "FlashAttention and Triton" §19.4-§19.6):
+//   per query row r:  O_r = sum_c exp(s_rc - m_r) V_c / l_r,
+//                     LSE_r = m_r + ln(l_r),  s = scale * q.k
+// with S and P held only in tensor memory (TMEM) and registers.
+//
+// CTA = one (batch*head, 256-row query block) = two 128-row query tiles.
+// Warp roles (12 warps):
+//   warp 0      TMA producer: Q tiles once, then K_j / V_j through a ring of
+//               STAGES shared-memory slots (full/empty mbarrier pairs).
+//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma:
+//                 S_t = Q_t K_j^T   (SS form, fp32 accumulator in TMEM)
+//                 O_t += P_t V_j    (TS form: P read from TMEM, V from smem)
+//               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the
+//               tensor core works on one query tile while the softmax warps
+//               work on the other.
+//   warps 4-7   softmax for query tile 0, one thread per row (TMEM lane);
+//   warps 8-11  softmax for query tile 1.
+// Online softmax ("Lesson 1" §3) in the log2 domain: x = s * scale*log2(e),
+// p = 2^(x - m_ref), l = l * 2^(m_ref_old - m_ref) + rowsum(p). The reference
+// max m_ref is only raised when the tile max exceeds it by more than
+// kRescaleLog2 (p <= 2^kRescaleLog2 meanwhile); O and l always share the same
+// m_ref, so the result is exact in real arithmetic (the argument of
+// "Lesson 1" §4: every term is normalised to one common max). When m_ref
+// moves, the row of O in TMEM is multiplied by 2^(m_old - m_new) before the
+// next P V product is issued. P is rounded to bf16 and written over the S
+// columns it came from (the A operand of the TS MMA).
+// Epilogue: O / l to bf16, LSE = (m_ref + log2 l) * ln 2, rows >= N skipped.
+//
+// Every mbarrier wait is bounded; on expiry the kernel records a timeout in
+// the status word, drains its in-flight TMA loads and MMAs, frees TMEM and
+// exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kRescaleLog2 = 8.0f;  // tolerated growth of the running max before O is rescaled
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128;  // query rows per tile (TMEM lanes)
+  static constexpr int QT = 2;    // query tiles per CTA
+  static constexpr int BN = 128;  // keys per KV tile
+  static constexpr int CH = D / 64;  // 128-byte column chunks per row
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int CHUNK_BYTES = 128 * 128;  // one 128-row x 128-byte swizzled chunk
+  static constexpr int TILE_BYTES = CH * CHUNK_BYTES;  // 128 rows x D bf16
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QT * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
+  static constexpr int NBAR = 1 + 4 * STAGES + 3 * QT + 1;
+  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // TMEM columns: S_t at 128*t, O_t at 256 + D*t
+  static constexpr uint32_t S_COL(int t) { return 128u * t; }
+  static constexpr uint32_t O_COL(int t) { return 256u + (uint32_t)D * t; }
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  // barrier indices
+  const uint32_t bar0 = smem_u32(bars);
+  auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  const int B_QFULL = 0;
+  const int B_KFULL = 1, B_VFULL = 1 + C::STAGES, B_KEMPTY = 1 + 2 * C::STAGES,
+            B_VEMPTY = 1 + 3 * C::STAGES;
+  const int B_SFULL = 1 + 4 * C::STAGES, B_PFULL = B_SFULL + C::QT, B_ODONE = B_PFULL + C::QT;
+  const int B_DRAIN = B_ODONE + C::QT;
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int q0 = blockIdx.x * (C::BM * C::QT);
+  const int N = a.N;
+  const int n_kv = (N + C::BN - 1) / C::BN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(B_QFULL), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(BAR(B_KFULL + s), 1);
+      mbar_init(BAR(B_VFULL + s), 1);
+      mbar_init(BAR(B_KEMPTY + s), 1);
+      mbar_init(BAR(B_VEMPTY + s), 1);
+    }
+    for (int t = 0; t < C::QT; ++t) {
+      mbar_init(BAR(B_SFULL + t), 1);
+      mbar_init(BAR(B_PFULL + t), 128);
+      mbar_init(BAR(B_ODONE + t), 1);
+    }
+    mbar_init(BAR(B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32((const void*)tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tmQ);
+      tma_prefetch_desc(&a.tmK);
+      tma_prefetch_desc(&a.tmV);
+      mbar_arrive_expect_tx(BAR(B_QFULL), C::QT * C::TILE_BYTES);
+      for (int t = 0; t < C::QT; ++t)
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(sbase + C::OFF_Q + (t * C::CH + c) * C::CHUNK_BYTES, &a.tmQ, BAR(B_QFULL),
+                      c * 64, q0 + t * C::BM, bh);
+      int last_k[C::STAGES], last_v[C::STAGES];  // last tile loaded into each slot
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) last_k[s] = last_v[s] = -1;
+      for (int j = 0; j < n_kv; ++j) {
+        if (*abort_flag) break;
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        if (!mbar_wait(BAR(B_KEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(BAR(B_KFULL + s), C::TILE_BYTES);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmK,
+                      BAR(B_KFULL + s), c * 64, j * C::BN, bh);
+        last_k[s] = j;
+        if (!mbar_wait(BAR(B_VEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(BAR(B_VFULL + s), C::TILE_BYTES);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmV,
+                      BAR(B_VFULL + s), c * 64, j * C::BN, bh);
+        last_v[s] = j;
+      }
+      // drain: the last load issued into each slot must have landed before exit
+      mbar_wait(BAR(B_QFULL), 0, a.status, a.wait_limit_ns);
+#pragma unroll
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (last_k[s] >= 0)
+          mbar_wait(BAR(B_KFULL + s), (last_k[s] / C::STAGES) & 1, a.status, a.wait_limit_ns);
+        if (last_v[s] >= 0)
+          mbar_wait(BAR(B_VFULL + s), (last_v[s] / C::STAGES) & 1, a.status, a.wait_limit_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      auto issue_s = [&](int t, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sbase + C::OFF_Q + t * C::TILE_BYTES + off, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + s * C::TILE_BYTES + off, 16, 1024);
+          mma_ss(tmem + C::S_COL(t), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int s, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+          const uint64_t bd =
+              sdesc_sw128(sbase + C::OFF_V + s * C::TILE_BYTES + kk * 2048, C::CHUNK_BYTES, 1024);
+          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bd, idesc_o,
+                 (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(BAR(B_QFULL), 0, a.status, a.wait_limit_ns);
+      ok = ok && mbar_wait(BAR(B_KFULL + 0), 0, a.status, a.wait_limit_ns);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < C::QT; ++t) {
+          issue_s(t, 0);
+          mma_commit(BAR(B_SFULL + t));
+        }
+        mma_commit(BAR(B_KEMPTY + 0));
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (*abort_flag) { ok = false; break; }
+        const int s = j % C::STAGES;
+        const uint32_t ph = (j / C::STAGES) & 1;
+        const bool more = j + 1 < n_kv;
+        const int s1 = (j + 1) % C::STAGES;
+        const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
+        if (!mbar_wait(BAR(B_VFULL + s), ph, a.status, a.wait_limit_ns)) { ok = false; break; }
+        for (int t = 0; t < C::QT; ++t) {
+          if (!mbar_wait(BAR(B_PFULL + t), j & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          mma_commit(BAR(B_ODONE + t));
+          if (more) {
+            if (t == 0 && !mbar_wait(BAR(B_KFULL + s1), ph1, a.status, a.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, s1);
+            mma_commit(BAR(B_SFULL + t));
+          }
+        }
+        if (!ok) break;
+        mma_commit(BAR(B_VEMPTY + s));
+        if (more) mma_commit(BAR(B_KEMPTY + s1));
+      }
+      if (!ok) *abort_flag = 1;
+      // drain every MMA this thread issued before TMEM can be released
+      mma_commit(BAR(B_DRAIN));
+      mbar_wait(BAR(B_DRAIN), 0, a.status, a.wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;       // query tile of this warpgroup
+    const int wq = warp & 3;             // TMEM lane quarter
+    const int row_in_tile = wq * 32 + lane;
+    const int row = q0 + t * C::BM + row_in_tile;
+    const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t s_addr = lane_addr + C::S_COL(t);
+    const uint32_t o_addr = lane_addr + C::O_COL(t);
+    const float c2 = a.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+      bool w = mbar_wait(BAR(B_SFULL + t), j & 1, a.status, a.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      float x[128];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tmem_ld32(s_addr + 32 * q, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[32 * q + i] = __uint_as_float(r[i]) * c2;
+        }
+      }
+      const int valid = N - j * C::BN;
+      if (valid < C::BN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= valid) x[i] = -INFINITY;
+      }
+      float mt = x[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
+      const bool need = mt > m_ref + kRescaleLog2;
+      const float m_new = need ? mt : m_ref;
+      const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2_approx(x[2 * i] - m_new);
+        const float p1 = ex2_approx(x[2 * i + 1] - m_new);
+        sum += p0 + p1;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      l = l * alpha + sum;
+      m_ref = m_new;
+      if (j > 0) {
+        // P V of the previous tile must be complete before O is touched and
+        // before this tile's P is released.
+        w = mbar_wait(BAR(B_ODONE + t), (j - 1) & 1, a.status, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t r[32];
+            tmem_ld32(o_addr + 32 * q, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(o_addr + 32 * q, r);
+          }
+        }
+      }
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = pk[i];
+        tmem_st32(s_addr, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = pk[32 + i];
+        tmem_st32(s_addr + 32, r);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(B_PFULL + t));
+    }
+    if (ok && n_kv > 0) {
+      const bool w = mbar_wait(BAR(B_ODONE + t), (n_kv - 1) & 1, a.status, a.wait_limit_ns);
+      ok = __all_sync(0xffffffffu, w);
+    }
+    if (!ok) {
+      *abort_flag = 1;
+    } else {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow =
+          reinterpret_cast<__nv_bfloat16*>(a.O) + ((size_t)bh * N + (size_t)row) * D;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t r[32];
+        tmem_ld32(o_addr + 32 * q, r);
+        tmem_ld_wait();
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+            u.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+            u.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+            u.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+            dst[v] = u;
+          }
+        }
+      }
+      if (row < N) a.LSE[(size_t)bh * N + row] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, int BH, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.N + C::BM * C::QT - 1) / (C::BM * C::QT), BH);
+  fwd_bf16_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st) {
+  if (d == 128) return launch_fwd_d<128>(a, BH, st);
+  if (d == 64) return launch_fwd_d<64>(a, BH, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

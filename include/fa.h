@@ -1,0 +1,120 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused exact-attention library.
+ *
+ * The library computes exact scaled-dot-product attention
+ *     O = softmax(scale * Q K^T) V
+ * as one fused kernel per call: Q, K, V are tiled, the scores S and the
+ * probabilities P never reach global memory, and an online softmax (running
+ * row max m and denominator l, the partial O rescaled when the max moves) is
+ * kept per query row. This is the algorithm of "Lesson 1: FlashAttention core
+ * idea" §3-§4 and of "FlashAttention and Triton" §19.4-§19.6. The backward
+ * pass keeps only one number per query row from the forward pass (the
+ * log-sum-exp, "Lesson 1" §5) and recomputes S and P tile by tile.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are dense, contiguous, row-major [B, H, N, d] (d fastest);
+ *    per-row statistics are [B, H, N] float32.
+ *  - Every pointer argument is a DEVICE pointer (cudaMalloc / PyTorch CUDA
+ *    memory on the current device) unless stated otherwise. The caller owns
+ *    all buffers and the stream; the library allocates no device memory and
+ *    keeps no pointer after the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Work is enqueued asynchronously; FA_OK means "validated and
+ *    launched", not "finished".
+ *  - No call throws; errors are returned as fa_status. Arguments are validated
+ *    before anything is launched: on any error nothing is enqueued.
+ *  - Attention is non-causal, without mask or dropout.
+ *
+ * dtypes and head sizes
+ *  - FA_BF16: bf16 Q/K/V/O/dO/dQ/dK/dV, float32 accumulation, d in {64, 128}.
+ *    Runs on the tcgen05 tensor cores. Pointers 16-byte aligned.
+ *  - FA_F32 : float32 everything, 1 <= d <= 128, CUDA-core FFMA arithmetic.
+ *    Pointers 4-byte aligned.
+ *  - Any N >= 1 (ragged last tiles are masked), B >= 1, H >= 1,
+ *    B*H*N*d < 2^31 elements per tensor.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, non-positive size, bad scale, small workspace */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. bf16 with d not in {64,128}) */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed */
+  FA_ERR_TIMEOUT = 4      /* a kernel gave up on a bounded wait (reported by fa_check_device_status) */
+} fa_status;
+
+typedef enum { FA_F32 = 0, FA_BF16 = 1 } fa_dtype;
+
+/*
+ * Forward pass.  "Lesson 1" §4 (tiled forward, query tiles outer, key/value
+ * tiles inner, online softmax, O_i / l_i at the end).
+ *   Q, K, V : [B,H,N,d] inputs, dtype `dt`.
+ *   O       : [B,H,N,d] output, dtype `dt`.
+ *   LSE     : [B,H,N] float32 output, LSE = m + ln(l) of the scaled scores
+ *             scale * q.k (natural log). The backward pass consumes it.
+ *   scale   : finite, > 0 (the pages use 1/sqrt(d)).
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (before launch), FA_ERR_CUDA.
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int H, int N, int d, float scale, fa_dtype dt, void* stream);
+
+/*
+ * Bytes of device scratch that fa_bwd needs for this problem (0 on invalid
+ * arguments). The caller allocates it; its contents on entry do not matter.
+ * Holds the fp32 dQ accumulator and the per-row D = rowsum(dO o O) and
+ * LSE * log2(e) statistics.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt);
+
+/*
+ * Backward pass with recomputation.  "Lesson 1" §5: with P rebuilt from the
+ * saved statistics, dV = P^T dO, dP = dO V^T,
+ * dS = P o (dP - rowsum(dO o O)) * scale, dQ = dS K, dK = dS^T Q.
+ * (rowsum(dP o P) over a full row equals rowsum(dO o O) because O = P V.)
+ *   Q, K, V, O, dO : [B,H,N,d] inputs, dtype `dt` (O from fa_fwd).
+ *   LSE            : [B,H,N] float32 from fa_fwd.
+ *   dQ, dK, dV     : [B,H,N,d] outputs, dtype `dt`.
+ *   workspace      : device scratch of >= fa_bwd_workspace_bytes() bytes,
+ *                    256-byte aligned, not used by another call in flight.
+ * Errors: as fa_fwd, plus FA_ERR_INVALID_ARG when the workspace is too small.
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, float scale, fa_dtype dt,
+                 void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device. Returns FA_ERR_TIMEOUT if any kernel launched
+ * since the last check abandoned a bounded wait (its outputs are then
+ * undefined), FA_ERR_CUDA if the stream reports an error, FA_OK otherwise.
+ */
+fa_status fa_check_device_status(void* stream);
+
+/*
+ * Test hook for the bounded-wait machinery: launches one block that waits on
+ * a shared-memory barrier nothing will ever arrive at, giving up after
+ * `limit_ns` nanoseconds (clamped to [1e3, 2e9]) and recording FA_ERR_TIMEOUT
+ * in the device status word, exactly as the attention kernels do. Lets a test
+ * observe the timeout path without hanging or faulting the GPU.
+ */
+fa_status fa_debug_timeout_probe(long long limit_ns, void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fa_status_string(fa_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

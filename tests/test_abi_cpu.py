@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+function that include/fa.h declares, and rejects bad arguments before touching
+the GPU (these calls return from validation without any CUDA call)."""
+import ctypes
+import os
+
+import pytest
+
+import exact_attention_30_gb300 as fa
+from exact_attention_30_gb300 import build as fa_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.library_path()):
+        fa_build.build()
+    return fa.load_library()
+
+
+def test_header_declares_expected_entry_points():
+    names = fa.header_functions()
+    for n in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_check_device_status",
+              "fa_status_string", "fa_version", "fa_debug_timeout_probe"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in fa.header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert fa.fa_status_string(fa.FA_OK) == "FA_OK"
+    for code in (fa.FA_ERR_INVALID_ARG, fa.FA_ERR_UNSUPPORTED, fa.FA_ERR_CUDA, fa.FA_ERR_TIMEOUT):
+        assert fa.fa_status_string(code).startswith("FA_ERR_")
+    assert fa.fa_version() >= 100
+
+
+def test_workspace_size_is_host_only(lib):
+    n = fa.fa_bwd_workspace_bytes(2, 16, 4096, 128)
+    # dQ accumulator (fp32) + two fp32 row statistics, rows padded to 128
+    assert n >= 2 * 16 * 4096 * 128 * 4 + 2 * 2 * 16 * 4096 * 4
+    assert n % 256 == 0
+    assert lib.fa_bwd_workspace_bytes(0, 1, 1, 64, fa.FA_BF16) == 0
+    assert lib.fa_bwd_workspace_bytes(1, 1, 1, 96, fa.FA_BF16) == 0  # unsupported d
+    assert lib.fa_bwd_workspace_bytes(1, 1, 1000, 64, fa.FA_F32) >= 4000
+
+
+FAKE = 0x10000  # an aligned non-null value: never dereferenced, validation fails first
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0.125, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 0, 1, 16, 64, 0.125, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 64, 0.125, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0.0, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, float("nan"), fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 96, 0.125, fa.FA_BF16), fa.FA_ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 256, 0.125, fa.FA_F32), fa.FA_ERR_UNSUPPORTED),
+    ((FAKE + 8, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0.125, fa.FA_BF16), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 16, 64, 0.125, 7), fa.FA_ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 70000, 1, 16, 64, 0.125, fa.FA_BF16), fa.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_bad_arguments_before_launch(lib, args, code):
+    assert lib.fa_fwd(*args, None) == code
+
+
+def test_bwd_rejects_small_workspace_and_nulls(lib):
+    ws = fa.fa_bwd_workspace_bytes(1, 2, 300, 64)
+    ptrs = [FAKE] * 10
+    assert lib.fa_bwd(*ptrs, ws - 1, 1, 2, 300, 64, 0.125, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    bad = list(ptrs)
+    bad[6] = 0  # dQ
+    assert lib.fa_bwd(*bad, ws, 1, 2, 300, 64, 0.125, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    bad = list(ptrs)
+    bad[9] = FAKE + 16  # workspace not 256-byte aligned
+    assert lib.fa_bwd(*bad, ws, 1, 2, 300, 64, 0.125, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.fa_fwd(q, q, q)
