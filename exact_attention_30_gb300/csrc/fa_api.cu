@@ -44,12 +44,12 @@ bool get_encode_fn() {
   return true;
 }
 
-// [BH, N, d] bf16 viewed as 3-D (d, N, BH); box 64 x 128 x 1, 128-byte swizzle.
-// Rows past N within a head read as zero.
-bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d) {
+// [BH, N, d] bf16 viewed as 3-D (d, N, BH); box 64 x box_rows x 1, 128-byte
+// swizzle. Rows past N within a head read as zero.
+bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -172,8 +172,8 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
   if (!status) return FA_ERR_CUDA;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_bhnd_bf16(&a.tmQ, Q, BH, N, d) || !encode_bhnd_bf16(&a.tmK, K, BH, N, d) ||
-      !encode_bhnd_bf16(&a.tmV, V, BH, N, d))
+  if (!encode_bhnd_bf16(&a.tmQ, Q, BH, N, d, 128) || !encode_bhnd_bf16(&a.tmK, K, BH, N, d, 128) ||
+      !encode_bhnd_bf16(&a.tmV, V, BH, N, d, 128))
     return FA_ERR_CUDA;
   a.O = O;
   a.LSE = LSE;
@@ -220,8 +220,10 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   if (!status) return FA_ERR_CUDA;
   BwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_bhnd_bf16(&a.tmQ, Q, BH, N, d) || !encode_bhnd_bf16(&a.tmK, K, BH, N, d) ||
-      !encode_bhnd_bf16(&a.tmV, V, BH, N, d) || !encode_bhnd_bf16(&a.tmdO, dO, BH, N, d))
+  // query-side tiles (Q, dO) are bwd_query_tile(d) rows, key-side tiles 128 rows
+  const int qrows = bwd_query_tile(d);
+  if (!encode_bhnd_bf16(&a.tmQ, Q, BH, N, d, qrows) || !encode_bhnd_bf16(&a.tmK, K, BH, N, d, 128) ||
+      !encode_bhnd_bf16(&a.tmV, V, BH, N, d, 128) || !encode_bhnd_bf16(&a.tmdO, dO, BH, N, d, qrows))
     return FA_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   a.O = O;
