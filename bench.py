@@ -1,0 +1,451 @@
+#!/usr/bin/env python
+"""Throughput of the fused exact-attention hot path on one (or N) GB300.
+
+One step = the whole path on one synthetic batch: fa_fwd (O, LSE) then the
+three backward stages (preprocess, recompute main kernel, dQ convert), bf16,
+B=2 H=16 N=4096 d=128, non-causal, inputs i.i.d. N(0,1) rounded to bf16.
+FLOPs per step: 4*B*H*N^2*d (forward) + 2.5x that (backward).
+
+Arms:
+  default           our CUDA kernels through the C ABI; prints one JSON line.
+  --impl reference  the fp64 CPU oracle on the host cores, on a bounded sample
+                    of the same workload (a strip of query rows of one head).
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and a
+device synchronize. L2 is flushed (256 MiB write) before every step; each step
+is timed with CUDA events on the launching stream, and so is every kernel
+launch of the dominant kernel. Under torchrun each rank runs its own batch
+(weak scaling, no collective on the data path); rank 0 reports the max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 (bf16) and % of tensor-core peak"
+B, H, N, D = 2, 16, 4096, 128
+WORKLOAD = f"fwd+bwd bf16 B={B} H={H} N={N} d={D} non-causal"
+FWD_FLOPS = 4.0 * B * H * N * N * D
+BWD_FLOPS = 2.5 * FWD_FLOPS
+STEP_FLOPS = FWD_FLOPS + BWD_FLOPS
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "bwd_main_traffic.txt")
+BWD_SOURCE = os.path.join(ROOT, "exact_attention_30_gb300", "csrc", "attn_bwd_bf16.cu")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="fa", choices=["fa", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--heads", type=int, default=None,
+                   help="override H (smaller profiling captures); the JSON line names the change")
+    args = p.parse_args()
+    if args.heads is not None:
+        global H, WORKLOAD, FWD_FLOPS, BWD_FLOPS, STEP_FLOPS
+        H = args.heads
+        WORKLOAD = f"fwd+bwd bf16 B={B} H={H} N={N} d={D} non-causal"
+        FWD_FLOPS = 4.0 * B * H * N * N * D
+        BWD_FLOPS = 2.5 * FWD_FLOPS
+        STEP_FLOPS = FWD_FLOPS + BWD_FLOPS
+    return args
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "hbm_gbs": float(pk["hbm_gbs"])}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
+
+
+def read_traffic():
+    """DRAM bytes per launch of the backward main kernel from the committed ncu
+    summary, or None when the kernel source changed since it was captured."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 2 and not line.startswith("#"):
+                    fields[parts[0]] = parts[1]
+        with open(BWD_SOURCE, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if fields.get("source_sha256") != sha:
+            return None
+        return float(fields["dram_bytes_per_launch_full_size"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, uuid: str | None):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_bench_clocks_{os.getpid()}.csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t_start = None
+
+    def wait_first_sample(self, timeout=3.0):
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.05)
+
+    def mark(self):
+        self.t_mark = os.path.getsize(self.path) if self.proc is not None else 0
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        with open(self.path) as f:
+            f.seek(self.t_mark)
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.remove(self.path)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------- oracle arm
+def oracle_step_rows(q64, k64, v64, do64, scale, rows):
+    """fwd + bwd of the oracle restricted to a strip of query rows of one head.
+
+    The backward is a sum over query rows, so a strip gives exact dQ rows and
+    that strip's exact contribution to dK and dV."""
+    from oracle import attention_bwd, attention_fwd
+    qs, dos = q64[rows], do64[rows]
+    attention_fwd(qs, k64, v64, scale)
+    attention_bwd(qs, k64, v64, dos, scale)
+    return len(rows) * N * D * (4.0 + 10.0)  # fwd 4*R*N*d + bwd 2.5x
+
+
+def oracle_sample_inputs(seed=0):
+    import numpy as np
+    import torch
+
+    from exact_attention_30_gb300.inputs import random_qkv
+    q, k, v, do = random_qkv(1, 1, N, D, torch.bfloat16, seed=seed)
+    f = lambda t: t[0, 0].to(torch.float64).numpy()
+    return f(q), f(k), f(v), f(do), np.float32(1 / math.sqrt(D))
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            try:
+                return int(os.environ[var])
+            except ValueError:
+                pass
+    return os.cpu_count()
+
+
+def cpu_baseline(seconds: float):
+    """Time the oracle on the host cores for about `seconds`: fwd+bwd of
+    256-row query strips of successive seeded heads of the workload's shape."""
+    flops, rows_done, heads = 0.0, 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        q64, k64, v64, do64, scale = oracle_sample_inputs(seed=heads)
+        heads += 1
+        for r0 in range(0, N, 256):
+            if time.perf_counter() - t0 >= seconds:
+                break
+            rows = list(range(r0, min(r0 + 256, N)))
+            flops += oracle_step_rows(q64, k64, v64, do64, scale, rows)
+            rows_done += len(rows)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, fwd+bwd of {rows_done} query rows (256-row strips over "
+                      f"{heads} seeded head(s) of N={N}, d={D}) against all {N} keys, {dt:.1f} s "
+                      f"(input generation included)"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    q64, k64, v64, do64, scale = oracle_sample_inputs()
+    # size the strip so that the whole run stays within about two minutes
+    t0 = time.perf_counter()
+    oracle_step_rows(q64, k64, v64, do64, scale, list(range(64)))
+    t64 = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    R = int(max(8, min(N, 64 * budget / max(t64, 1e-6))))
+    R = 1 << int(math.log2(R))
+    for i in range(args.warmup):
+        oracle_step_rows(q64, k64, v64, do64, scale, list(range(R)))
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        r0 = (i * R) % N
+        rows = [(r0 + t) % N for t in range(R)]
+        t0 = time.perf_counter()
+        flops = oracle_step_rows(q64, k64, v64, do64, scale, rows)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    sample = (f"per step: fp64 numpy oracle fwd+bwd of {R} query rows of one head "
+              f"(N={N}, d={D}) against all keys")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D,
+                   "sample_rows_per_step": R, "flops_per_step_sample": flops},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import exact_attention_30_gb300 as fa
+    from exact_attention_30_gb300.inputs import random_qkv
+
+    fa.load_library()
+    stream = torch.cuda.current_stream(dev)
+    scale = 1 / math.sqrt(D)
+    q_h, k_h, v_h, do_h = random_qkv(B, H, N, D, torch.bfloat16, seed=rank)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def bwd_stage(stage):
+        fa.fa_bwd_stage(stage, q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+        if ev is not None:
+            ev[1].record(stream)
+        bwd_stage(fa.FA_BWD_PREPROCESS)
+        if ev is not None:
+            ev[2].record(stream)
+        bwd_stage(fa.FA_BWD_MAIN)
+        if ev is not None:
+            ev[3].record(stream)
+        bwd_stage(fa.FA_BWD_DQ_CONVERT)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fa.fa_check_device_status(dev) != fa.FA_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(dev.index, uuid) if rank == 0 else None
+    if sampler:
+        sampler.wait_first_sample()
+        sampler.mark()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    status = fa.fa_check_device_status(dev)
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)}")
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in events]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in events]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in events]
+    main_ms = [e[2].elapsed_time(e[3]) for e in events]
+    conv_ms = [e[3].elapsed_time(e[4]) for e in events]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    # end to end through the public API with pinned host buffers
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv, hdo = pin(q_h), pin(k_h), pin(v_h), pin(do_h)
+    hdq, hdk, hdv = (torch.empty(q_h.shape, dtype=q_h.dtype).pin_memory() for _ in range(3))
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+        fa.fa_bwd(q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    nbytes = q_h.numel() * q_h.element_size()
+
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return 0
+
+    peaks, peak_src = read_peaks()
+    peak = peaks["bf16_tflops"]
+    mean = lambda xs: sum(xs) / len(xs)
+    main_avg = mean(main_ms)
+    achieved = BWD_FLOPS / (main_avg * 1e-3) / 1e12
+    traffic = read_traffic()
+    fwd_avg = mean(fwd_ms)
+    value = world * STEP_FLOPS / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D,
+                   "flops_per_step": STEP_FLOPS,
+                   "l2": "flushed before every step (256 MiB write, outside the per-step events)",
+                   "parallelism": f"replicas x{world}, independent batches, no collective"},
+        "roofline": {"kernel": "bwd_main_kernel<128>", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
+                     "algorithmic_flops_per_launch": BWD_FLOPS},
+        "components": {
+            "fwd": {"kernel": "fwd_bf16_kernel<128>", "ms": fwd_avg,
+                    "tflops": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12,
+                    "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak},
+            "bwd_preprocess": {"ms": mean(pre_ms)},
+            "bwd_main": {"ms": main_avg, "tflops": achieved, "frac_of_peak": achieved / peak},
+            "bwd_dq_convert": {"ms": mean(conv_ms)},
+            "bwd_total": {"ms": mean(pre_ms) + main_avg + mean(conv_ms),
+                          "tflops": BWD_FLOPS / ((mean(pre_ms) + main_avg + mean(conv_ms)) * 1e-3) / 1e12},
+            "step_ms_median": statistics.median(step_ms),
+            "wall_ms_per_step_incl_flush": 1e3 * wall / args.steps,
+        },
+        "e2e": {"value": world * STEP_FLOPS / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 4 * nbytes,
+                "d2h_bytes_per_step": 3 * nbytes},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -21,14 +21,15 @@ import re
 import torch
 
 __all__ = [
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_check_device_status",
+    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes", "fa_check_device_status",
     "fa_debug_timeout_probe", "fa_status_string", "fa_version", "library_path", "load_library",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
-    "FA_F32", "FA_BF16", "FAError",
+    "FA_F32", "FA_BF16", "FAError", "FA_BWD_PREPROCESS", "FA_BWD_MAIN", "FA_BWD_DQ_CONVERT",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_F32, FA_BF16 = 0, 1
+FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
@@ -39,6 +40,7 @@ _SIGNATURES = {
     "fa_fwd": (_ci, [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
     "fa_bwd": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_bwd_stage": (_ci, [_ci] + [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_check_device_status": (_ci, [_vp]),
     "fa_debug_timeout_probe": (_ci, [ctypes.c_longlong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_ci]),
@@ -144,9 +146,7 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int, dtype=torch.bfloat16)
     return int(load_library().fa_bwd_workspace_bytes(B, H, N, d, code))
 
 
-def fa_bwd(q, k, v, o, do, lse, scale: float | None = None, workspace=None, dq=None, dk=None,
-           dv=None):
-    """Backward pass: returns (dQ, dK, dV), each like q."""
+def _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv):
     lib = load_library()
     _check(q, "q")
     for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
@@ -155,21 +155,36 @@ def fa_bwd(q, k, v, o, do, lse, scale: float | None = None, workspace=None, dq=N
     if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_cuda or not lse.is_contiguous():
         raise ValueError("lse must be contiguous float32 [B,H,N] on the same device")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    ws_bytes = fa_bwd_workspace_bytes(B, H, N, d, q.dtype)
     if workspace is None:
+        ws_bytes = fa_bwd_workspace_bytes(B, H, N, d, q.dtype)
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
     for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, q)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), B, H, N, d, scale, _dtype_code(q),
+            _stream_ptr(q.device))
     with torch.cuda.device(q.device):
-        rc = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                        workspace.data_ptr(), workspace.numel(), B, H, N, d, scale,
-                        _dtype_code(q), _stream_ptr(q.device))
-    _raise(rc, "fa_bwd")
+        if stage is None:
+            _raise(lib.fa_bwd(*args), "fa_bwd")
+        else:
+            _raise(lib.fa_bwd_stage(int(stage), *args), "fa_bwd_stage")
     return dq, dk, dv
+
+
+def fa_bwd(q, k, v, o, do, lse, scale: float | None = None, workspace=None, dq=None, dk=None,
+           dv=None):
+    """Backward pass: returns (dQ, dK, dV), each like q."""
+    return _bwd_call(None, q, k, v, o, do, lse, scale, workspace, dq, dk, dv)
+
+
+def fa_bwd_stage(stage: int, q, k, v, o, do, lse, scale: float | None = None, workspace=None,
+                 dq=None, dk=None, dv=None):
+    """One backward stage (FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT) on ``workspace``."""
+    return _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv)
 
 
 def fa_check_device_status(device=None) -> int:

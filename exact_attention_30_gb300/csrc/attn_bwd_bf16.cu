@@ -115,8 +115,11 @@ struct BwdCfg {
   static constexpr int BQ = DQ_T ? 64 : 128; // queries per streamed tile
   static constexpr int CH = D / 64;          // 128-byte chunks per K/V/Q/dO row
   static constexpr int QCH = BQ / 64;        // 128-byte chunks per P^T/dS^T row
-  static constexpr int STAGES = 2;
-  static constexpr int NPS = DQ_T ? 2 : 1;  // P^T/dS^T shared-memory buffers
+  // Q/dO ring depth: a slot is busy from the S^T prefetch of its tile until
+  // the dK/dV products one iteration later, so loads need >= 3 slots to run
+  // ahead of use; the P^T/dS^T tiles are single-buffered to make room.
+  static constexpr int STAGES = 3;
+  static constexpr int NPS = 1;  // P^T/dS^T shared-memory buffers
   static constexpr int KV_CHUNK = BK * 128;          // 16 KB
   static constexpr int Q_CHUNK = BQ * 128;           // 8 or 16 KB
   static constexpr int KV_TILE = CH * KV_CHUNK;
@@ -307,11 +310,11 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         if (!mbar_wait(BAR(B_PREADY + bp), php, a.status, a.wait_limit_ns)) { ok = false; break; }
         tc_fence_after();
         issue_acc(s, bp, i > 0);
+        mma_commit(BAR(B_QEMPTY + s));  // Q_i, dO_i, stats: last use was dK/dV
         if (!mbar_wait(BAR(B_DQEMPTY + b), ((i >> 1) & 1) ^ 1, a.status, a.wait_limit_ns)) { ok = false; break; }
         tc_fence_after();
         issue_dq(b, bp);
         mma_commit(BAR(B_DQFULL + b));
-        mma_commit(BAR(B_QEMPTY + s));
         mma_commit(BAR(B_PSEMPTY + bp));
       }
       if (ok) mma_commit(BAR(B_ACC));
@@ -363,15 +366,23 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         }
         uint32_t pk[32], dk[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int q = 64 * h + 2 * k;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * k]), c2, -lse2[q]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * k + 1]), c2, -lse2[q + 1]));
-          float d0 = p0 * (__uint_as_float(dr[2 * k]) - drow[q]) * scale;
-          float d1 = p1 * (__uint_as_float(dr[2 * k + 1]) - drow[q + 1]) * scale;
-          if (!key_live) { p0 = p1 = d0 = d1 = 0.f; }
-          pk[k] = pack_bf16x2(p0, p1);
-          dk[k] = pack_bf16x2(d0, d1);
+        for (int k4 = 0; k4 < 16; ++k4) {
+          const int q = 64 * h + 4 * k4;
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
+          const float4 d4 = *reinterpret_cast<const float4*>(drow + q);
+          const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dq[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            p[u] = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + u]), c2, -lq[u]));
+            ds[u] = p[u] * (__uint_as_float(dr[4 * k4 + u]) - dq[u]) * scale;
+            if (!key_live) p[u] = ds[u] = 0.f;
+          }
+          pk[2 * k4] = pack_bf16x2(p[0], p[1]);
+          pk[2 * k4 + 1] = pack_bf16x2(p[2], p[3]);
+          dk[2 * k4] = pack_bf16x2(ds[0], ds[1]);
+          dk[2 * k4 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
         // row r of a 128-byte-swizzled [128 x 64] bf16 tile: 16-byte chunk c at c ^ (r & 7)
         uint8_t* prow = pbuf + h * C::PS_CHUNK + r * 128;
@@ -464,37 +475,41 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BwdArgs& a, int BH, cudaStream_t st) {
+cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t st) {
   using C = BwdCfg<D>;
   static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
-  {
+  cudaError_t e = cudaSuccess;
+  if (stages & kStagePre) {
     constexpr int RPW = 32 / (D / 8);
     const long long rows = (long long)BH * a.Npad;
     const long long warps = (rows + RPW - 1) / RPW;
     const long long blocks = (warps * 32 + 255) / 256;
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, BH);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-  if (e != cudaSuccess) return e;
-  dim3 grid((a.N + C::BK - 1) / C::BK, BH);
-  bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
+  if (stages & kStageMain) {
+    e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.N + C::BK - 1) / C::BK, BH);
+    bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kStageConvert) {
     const long long groups = (long long)BH * a.N * (D / 8);
     dq_convert_kernel<D><<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(a, BH);
+    e = cudaGetLastError();
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, cudaStream_t st) {
-  if (d == 128) return launch_bwd_d<128>(a, BH, st);
-  if (d == 64) return launch_bwd_d<64>(a, BH, st);
+cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st) {
+  if (d == 128) return launch_bwd_d<128>(a, BH, stages, st);
+  if (d == 64) return launch_bwd_d<64>(a, BH, stages, st);
   return cudaErrorInvalidValue;
 }
 

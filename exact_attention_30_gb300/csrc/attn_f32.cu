@@ -262,10 +262,7 @@ bwd_dkdv_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
 }
 
 template <typename Kern>
-cudaError_t launch_smem(Kern kern, dim3 grid, size_t smem, cudaStream_t st) {
-  (void)kern;
-  (void)grid;
-  (void)st;
+cudaError_t set_smem(Kern kern, size_t smem) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
@@ -274,7 +271,7 @@ cudaError_t fwd_f32_dc(const float* Q, const float* K, const float* V, float* O,
                        int BH, int N, int d, float scale, cudaStream_t st) {
   const size_t smem = sizeof(float) * ((size_t)kWarps * d + (size_t)kTile * (d + 1) + (size_t)kTile * d);
   dim3 grid((N + kWarps - 1) / kWarps, BH);
-  cudaError_t e = launch_smem(fwd_f32_kernel<DC>, grid, smem, st);
+  cudaError_t e = set_smem(fwd_f32_kernel<DC>, smem);
   if (e != cudaSuccess) return e;
   fwd_f32_kernel<DC><<<grid, 32 * kWarps, smem, st>>>(Q, K, V, O, LSE, N, d, scale);
   return cudaGetLastError();
@@ -283,20 +280,25 @@ cudaError_t fwd_f32_dc(const float* Q, const float* K, const float* V, float* O,
 template <int DC>
 cudaError_t bwd_f32_dc(const float* Q, const float* K, const float* V, const float* O,
                        const float* dO, const float* LSE, float* dQ, float* dK, float* dV,
-                       float* Dws, int BH, int N, int d, float scale, cudaStream_t st) {
+                       float* Dws, int BH, int N, int d, float scale, unsigned stages,
+                       cudaStream_t st) {
   dim3 grid((N + kWarps - 1) / kWarps, BH);
-  bwd_pre_f32_kernel<<<grid, 32 * kWarps, 0, st>>>(O, dO, Dws, N, d);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (stages & kStagePre) {
+    bwd_pre_f32_kernel<<<grid, 32 * kWarps, 0, st>>>(O, dO, Dws, N, d);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (!(stages & kStageMain)) return cudaSuccess;  // the fp32 path has no separate convert
   const size_t smem_dq = sizeof(float) * (2 * (size_t)kWarps * d + 2 * (size_t)kTile * (d + 1));
-  e = launch_smem(bwd_dq_f32_kernel<DC>, grid, smem_dq, st);
+  e = set_smem(bwd_dq_f32_kernel<DC>, smem_dq);
   if (e != cudaSuccess) return e;
   bwd_dq_f32_kernel<DC><<<grid, 32 * kWarps, smem_dq, st>>>(Q, K, V, dO, LSE, Dws, dQ, N, d, scale);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem_kv =
       sizeof(float) * (2 * (size_t)kWarps * d + 2 * (size_t)kTile * (d + 1) + 2 * (size_t)kTile);
-  e = launch_smem(bwd_dkdv_f32_kernel<DC>, grid, smem_kv, st);
+  e = set_smem(bwd_dkdv_f32_kernel<DC>, smem_kv);
   if (e != cudaSuccess) return e;
   bwd_dkdv_f32_kernel<DC><<<grid, 32 * kWarps, smem_kv, st>>>(Q, K, V, dO, LSE, Dws, dK, dV, N, d,
                                                                scale);
@@ -314,10 +316,11 @@ cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float
 
 cudaError_t launch_bwd_f32(const float* Q, const float* K, const float* V, const float* O,
                            const float* dO, const float* LSE, float* dQ, float* dK, float* dV,
-                           float* Dws, int BH, int N, int d, float scale, cudaStream_t st) {
-  if (d <= 32) return bwd_f32_dc<1>(Q, K, V, O, dO, LSE, dQ, dK, dV, Dws, BH, N, d, scale, st);
-  if (d <= 64) return bwd_f32_dc<2>(Q, K, V, O, dO, LSE, dQ, dK, dV, Dws, BH, N, d, scale, st);
-  return bwd_f32_dc<4>(Q, K, V, O, dO, LSE, dQ, dK, dV, Dws, BH, N, d, scale, st);
+                           float* Dws, int BH, int N, int d, float scale, unsigned stages,
+                           cudaStream_t st) {
+  if (d <= 32) return bwd_f32_dc<1>(Q, K, V, O, dO, LSE, dQ, dK, dV, Dws, BH, N, d, scale, stages, st);
+  if (d <= 64) return bwd_f32_dc<2>(Q, K, V, O, dO, LSE, dQ, dK, dV, Dws, BH, N, d, scale, stages, st);
+  return bwd_f32_dc<4>(Q, K, V, O, dO, LSE, dQ, dK, dV, Dws, BH, N, d, scale, stages, st);
 }
 
 }  // namespace fa

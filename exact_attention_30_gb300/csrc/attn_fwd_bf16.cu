@@ -240,38 +240,53 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       bool w = mbar_wait(BAR(B_SFULL + t), j & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      float x[128];
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tmem_ld32(s_addr + 32 * q, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[32 * q + i] = __uint_as_float(r[i]) * c2;
-        }
-      }
+      // raw scores of this row: four 32-column loads, one wait
+      uint32_t r[128];
+      tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+      tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+      tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+      tmem_ld_wait();
       const int valid = N - j * C::BN;
       if (valid < C::BN) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
-          if (i >= valid) x[i] = -INFINITY;
+          if (i >= valid) r[i] = __float_as_uint(-INFINITY);
       }
-      float mt = x[0];
+      // row max with 8 independent chains (scale > 0 commutes with max)
+      float mx[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mt = fmaxf(mt, x[i]);
+      for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(r[u]);
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], mx[u + 4]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
       const bool need = mt > m_ref + kRescaleLog2;
       const float m_new = need ? mt : m_ref;
       const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-      float sum = 0.f;
-      uint32_t pk[64];
+      const float neg_m = -m_new;
+      // p = 2^(s*c2 - m_new), summed with 8 independent chains, rounded to
+      // bf16 and written over the first 64 S columns in two 32-column halves
+      // (S of this tile is already in registers).
+      float sm8[8];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(x[2 * i] - m_new);
-        const float p1 = ex2_approx(x[2 * i + 1] - m_new);
-        sum += p0 + p1;
-        pk[i] = pack_bf16x2(p0, p1);
+      for (int u = 0; u < 8; ++u) sm8[u] = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 64 * hh + 2 * i;
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c]), c2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c + 1]), c2, neg_m));
+          sm8[c & 7] += p0;
+          sm8[(c + 1) & 7] += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_addr + 32 * hh, pk);
       }
+      const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
       l = l * alpha + sum;
       m_ref = m_new;
       if (j > 0) {
@@ -283,28 +298,20 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
-            uint32_t r[32];
-            tmem_ld32(o_addr + 32 * q, r);
+            uint32_t o[32];
+            tmem_ld32(o_addr + 32 * q, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(o_addr + 32 * q, r);
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(o_addr + 32 * q, o);
           }
         }
-      }
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = pk[i];
-        tmem_st32(s_addr, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = pk[32 + i];
-        tmem_st32(s_addr + 32, r);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(B_PFULL + t));
     }
+    tmem_st_wait();  // no TMEM store may be in flight when the loop is left early
     if (ok && n_kv > 0) {
       const bool w = mbar_wait(BAR(B_ODONE + t), (n_kv - 1) & 1, a.status, a.wait_limit_ns);
       ok = __all_sync(0xffffffffu, w);

@@ -189,10 +189,13 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt) {
   return bwd_layout(B, H, N, d, dt).total;
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
-                 size_t workspace_bytes, int B, int H, int N, int d, float scale, fa_dtype dt,
-                 void* stream) {
+}  // extern "C"
+
+namespace {
+fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                   void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                   float scale, fa_dtype dt, void* stream) {
   fa_status s = check_shape(B, H, N, d, scale, dt);
   if (s != FA_OK) return s;
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
@@ -211,7 +214,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                           static_cast<const float*>(V), static_cast<const float*>(O),
                           static_cast<const float*>(dO), LSE, static_cast<float*>(dQ),
                           static_cast<float*>(dK), static_cast<float*>(dV),
-                          static_cast<float*>(workspace), BH, N, d, scale, st) == cudaSuccess
+                          static_cast<float*>(workspace), BH, N, d, scale, stages, st) == cudaSuccess
                ? FA_OK
                : FA_ERR_CUDA;
   }
@@ -241,8 +244,35 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.wait_limit_ns = kDefaultWaitLimitNs;
-  return launch_bwd_bf16(a, BH, d, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, float scale, fa_dtype dt,
+                 void* stream) {
+  return bwd_impl(kStageAll, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H,
+                  N, d, scale, dt, stream);
+}
+
+fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       float scale, fa_dtype dt, void* stream) {
+  unsigned bits;
+  switch (stage) {
+    case FA_BWD_PREPROCESS: bits = kStagePre; break;
+    case FA_BWD_MAIN: bits = kStageMain; break;
+    case FA_BWD_DQ_CONVERT: bits = kStageConvert; break;
+    default: return FA_ERR_INVALID_ARG;
+  }
+  return bwd_impl(bits, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d,
+                  scale, dt, stream);
+}
+
 
 fa_status fa_check_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -19,9 +19,12 @@ int* device_status_ptr();
 // ---- fp32 CUDA-core path (attn_f32.cu) ----
 cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
                            int BH, int N, int d, float scale, cudaStream_t st);
+// Backward stage bits: preprocess, main, dQ convert.
+enum : unsigned { kStagePre = 1u, kStageMain = 2u, kStageConvert = 4u, kStageAll = 7u };
 cudaError_t launch_bwd_f32(const float* Q, const float* K, const float* V, const float* O,
                            const float* dO, const float* LSE, float* dQ, float* dK, float* dV,
-                           float* Dws, int BH, int N, int d, float scale, cudaStream_t st);
+                           float* Dws, int BH, int N, int d, float scale, unsigned stages,
+                           cudaStream_t st);
 
 // ---- bf16 tcgen05 path ----
 // Tensor maps describe one [BH, N, d] bf16 tensor as 3-D (d, N, BH) with
@@ -54,7 +57,7 @@ struct BwdArgs {
   int* status;
   unsigned long long wait_limit_ns;
 };
-cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, cudaStream_t st);
+cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
 // Row padding used by the bf16 backward workspace.
 constexpr int kBwdRowPad = 128;
 // Query rows per streamed tile of the bf16 backward kernel (its Q/dO TMA box

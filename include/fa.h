@@ -91,6 +91,25 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  void* stream);
 
 /*
+ * One stage of fa_bwd, for callers that schedule or time the stages
+ * separately. Same arguments and validation as fa_bwd, plus `stage`:
+ *   FA_BWD_PREPROCESS (0): D = rowsum(dO o O) and LSE * log2(e) per row into
+ *                          the workspace; zero the workspace's dQ accumulator.
+ *   FA_BWD_MAIN       (1): recompute P tile by tile; write dK, dV; add dQ
+ *                          into the workspace accumulator. Needs stage 0 done.
+ *   FA_BWD_DQ_CONVERT (2): workspace dQ accumulator -> dQ in dtype `dt`.
+ *                          Needs stage 1 done.
+ * Stages run in that order on one workspace; fa_bwd == stages 0, 1, 2.
+ * Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for an unknown stage.
+ */
+typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_MAIN = 1, FA_BWD_DQ_CONVERT = 2 } fa_bwd_stage_id;
+
+fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, const void* O,
+                       const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       float scale, fa_dtype dt, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device. Returns FA_ERR_TIMEOUT if any kernel launched
  * since the last check abandoned a bounded wait (its outputs are then
