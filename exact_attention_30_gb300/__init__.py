@@ -41,6 +41,7 @@ _SIGNATURES = {
     "fa_bwd_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
     "fa_bwd": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_stage": (_ci, [_ci] + [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_bwd_noalloc": (_ci, [_vp] * 9 + [_ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_check_device_status": (_ci, [_vp]),
     "fa_debug_timeout_probe": (_ci, [ctypes.c_longlong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_ci]),

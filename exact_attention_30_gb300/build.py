@@ -28,6 +28,7 @@ SOURCES = [
     ("attn_f32.cu", []),
     ("attn_fwd_bf16.cu", []),
     ("attn_bwd_bf16.cu", []),
+    ("fa_noalloc.cu", []),
 ]
 
 

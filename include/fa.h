@@ -110,6 +110,27 @@ fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, c
                        float scale, fa_dtype dt, void* stream);
 
 /*
+ * fa_bwd without a caller-provided workspace, for callers that cannot
+ * allocate device memory (for example code running inside a host application
+ * that owns all device memory through its own pool, or a serving path where
+ * cudaMalloc is not allowed). The paper has no counterpart to this entry point:
+ * it is a deployment convenience around fa_bwd.
+ * Same arguments, results and errors as fa_bwd, minus the workspace. The
+ * scratch is one library-owned device array of
+ * FA_BWD_NOALLOC_MAX_WORKSPACE_BYTES per device, held until process exit;
+ * problems needing more (fa_bwd_workspace_bytes) return FA_ERR_UNSUPPORTED
+ * without launching. All calls on a device share that array: calls whose
+ * kernels may overlap on the GPU race and must be ordered by the caller. The
+ * first call on each device looks up the array's address; make it before any
+ * stream capture. Allocates nothing.
+ */
+#define FA_BWD_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)32 << 20)
+
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                         int B, int H, int N, int d, float scale, fa_dtype dt, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device. Returns FA_ERR_TIMEOUT if any kernel launched
  * since the last check abandoned a bounded wait (its outputs are then
