@@ -14,20 +14,23 @@
 //                a multiple of 128: D = 0, LSE*log2(e) = +inf past N, which
 //                makes P = 0 there), and zero the fp32 dQ accumulator.
 //  2. bwd_main:  one CTA per (batch*head, 128-key tile j); K_j, V_j stay in
-//                shared memory while the query tiles i stream through a TMA
+//                shared memory while 128-query tiles i stream through a TMA
 //                ring. All products run on tcgen05 with fp32 accumulators in
-//                TMEM, keys on the TMEM lanes:
-//                  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T   (recompute)
-//                  dV += P^T dO_i,   dK += dS^T Q_i      (stay in TMEM)
-//                  dQ_i (+)= dS K_j  -> fp32 atomics into the accumulator
-//                The softmax warpgroup (one thread per key) turns S^T, dP^T
-//                into bf16 P^T and dS^T tiles in swizzled shared memory,
-//                which feed both the dV/dK and the dQ products. S^T/dP^T of
-//                the next query tile are computed while it works.
+//                TMEM (every MMA M = N = 128):
+//                  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T   (recompute; keys on lanes)
+//                  dV += P^T dO_i (P^T read from TMEM), dK += dS^T Q_i
+//                  dQ_i^T = K_j^T dS^T (d = 128) or dQ_i = dS K_j (d = 64)
+//                  -> fp32 atomics
+//                A softmax warpgroup (one thread per key) first writes bf16
+//                P^T over the S^T columns, then, once dP^T is there, writes
+//                bf16 dS^T into a swizzled shared-memory tile that feeds both
+//                dK (K-major view) and dQ (MN-major view). dQ_i is computed
+//                into the dP^T columns; a dQ warpgroup reads it out and adds
+//                it to the accumulator with 16-byte atomics. Per query tile the
+//                MMA order is dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1), so the
+//                next tile's recompute overlaps this tile's softmax.
 //  3. dq_convert: fp32 accumulator -> bf16 dQ.
-// d = 128 uses 64-query tiles and computes dQ^T = K_j^T dS^T (M = d);
-// d = 64 uses 128-query tiles and computes dQ = dS K_j (M = queries); both
-// keep every TMEM operand at M = 128 within 512 columns.
+// TMEM (512 columns): S^T|P^T, dP^T|dQ, dV, dK.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -110,62 +113,64 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, int BH
 // ----------------------------------------------------------------------------
 template <int D>
 struct BwdCfg {
-  static constexpr bool DQ_T = (D == 128);   // compute dQ^T (M = d) instead of dQ (M = queries)
-  static constexpr int BK = 128;             // keys per CTA (TMEM lanes)
-  static constexpr int BQ = DQ_T ? 64 : 128; // queries per streamed tile
-  static constexpr int CH = D / 64;          // 128-byte chunks per K/V/Q/dO row
-  static constexpr int QCH = BQ / 64;        // 128-byte chunks per P^T/dS^T row
-  // Q/dO ring depth: a slot is busy from the S^T prefetch of its tile until
-  // the dK/dV products one iteration later, so loads need >= 3 slots to run
-  // ahead of use; the P^T/dS^T tiles are single-buffered to make room.
-  static constexpr int STAGES = 3;
-  static constexpr int NPS = 1;  // P^T/dS^T shared-memory buffers
-  static constexpr int KV_CHUNK = BK * 128;          // 16 KB
-  static constexpr int Q_CHUNK = BQ * 128;           // 8 or 16 KB
-  static constexpr int KV_TILE = CH * KV_CHUNK;
-  static constexpr int Q_TILE = CH * Q_CHUNK;
-  static constexpr int PS_CHUNK = BK * 128;          // 16 KB: [128 keys][64 queries] bf16
-  static constexpr int PS_TILE = QCH * PS_CHUNK;
-  static constexpr int STAT_BYTES = 2 * BQ * 4;      // lse2 + D for one query tile
+  static constexpr int BK = 128;  // keys per CTA: TMEM lanes of S^T, dP^T, dV, dK
+  static constexpr int BQ = 128;  // queries per streamed tile
+  // d = 128 computes dQ^T = K^T dS^T (d on the TMEM lanes) so that a warp's
+  // fp32 atomics cover one contiguous 128-byte row segment; d = 64 computes
+  // dQ = dS K (queries on the lanes; an M = 64 product would be needed otherwise)
+  static constexpr bool DQ_T = (D == 128);
+  static constexpr int CH = D / 64;                  // 128-byte chunks per K/V/Q/dO row
+  static constexpr int STAGES = (D == 128) ? 2 : 3;  // Q/dO ring depth
+  static constexpr int ROW_CHUNK = 128 * 128;        // 128 rows x 128 bytes, swizzled
+  static constexpr int TILE = CH * ROW_CHUNK;        // 128 rows x D bf16
+  static constexpr int DS_TILE = 2 * ROW_CHUNK;      // dS^T: [128 keys][128 queries] bf16
+  static constexpr int STAT_BYTES = 2 * BQ * 4;      // LSE*log2(e) and D of one query tile
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_TILE;
-  static constexpr int OFF_Q = OFF_V + KV_TILE;
-  static constexpr int OFF_DO = OFF_Q + STAGES * Q_TILE;
-  static constexpr int OFF_P = OFF_DO + STAGES * Q_TILE;      // NPS buffers
-  static constexpr int OFF_DS = OFF_P + NPS * PS_TILE;        // NPS buffers
-  static constexpr int OFF_STAT = OFF_DS + NPS * PS_TILE;     // STAGES x STAT_BYTES
+  static constexpr int OFF_V = OFF_K + TILE;
+  static constexpr int OFF_DS = OFF_V + TILE;
+  static constexpr int OFF_Q = OFF_DS + DS_TILE;
+  static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
+  static constexpr int OFF_STAT = OFF_DO + STAGES * TILE;
   static constexpr int OFF_BAR = OFF_STAT + STAGES * STAT_BYTES;
-  // barriers: kv_full, q_full[S], qdo_empty[S], s_full, s_consumed, p_ready[2],
-  //           pds_empty[2], dq_full[2], dq_empty[2], acc_done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 2;
+  // barriers: kv_full, q_full[S], q_empty[S], s_full, dp_full, pt_ready, ds_ready,
+  //           ds_empty, dq_full, dq_empty, acc_done, drain
+  static constexpr int NBAR = 1 + 2 * STAGES + 9;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
-  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;
+  static constexpr int SMEM_MAX = 227 * 1024;
+  // request 1 KB of alignment slack when it fits; the kernel checks alignment
+  static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 <= SMEM_MAX) ? SMEM_BYTES + 1024 : SMEM_MAX;
   static constexpr int THREADS = 384;
-  // TMEM columns
+  // TMEM columns: S^T (P^T as bf16 in its first 64), dP^T (dQ after dP^T is
+  // consumed), dV, dK.
   static constexpr uint32_t COL_S = 0;
-  static constexpr uint32_t COL_DP = BQ;
-  static constexpr int DQC = DQ_T ? BQ : D;  // columns of one dQ buffer
-  static constexpr uint32_t COL_DQ = 2 * BQ;
-  static constexpr uint32_t COL_DV = 2 * BQ + 2 * DQC;
-  static constexpr uint32_t COL_DK = COL_DV + D;
+  static constexpr uint32_t COL_DP = 128;
+  static constexpr uint32_t COL_DV = 256;
+  static constexpr uint32_t COL_DK = 256 + D;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(COL_DK + D <= 512, "TMEM budget");
+  static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= SMEM_MAX, "shared memory budget");
   static_assert(BQ == bwd_query_tile(D), "host tensor-map box height");
 };
 
 template <int D>
 __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+  if (pad + C::SMEM_BYTES > (uint32_t)C::SMEM_ALLOC) {
+    // cannot place the swizzled tiles: report and leave before touching anything
+    if (threadIdx.x == 0) report_status(a.status, kStatusTimeout);
+    return;
+  }
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   const int B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + C::STAGES, B_SFULL = 1 + 2 * C::STAGES,
-            B_SCONS = B_SFULL + 1, B_PREADY = B_SCONS + 1, B_PSEMPTY = B_PREADY + 2,
-            B_DQFULL = B_PSEMPTY + 2, B_DQEMPTY = B_DQFULL + 2, B_ACC = B_DQEMPTY + 2,
-            B_DRAIN = B_ACC + 1;
+            B_DPFULL = B_SFULL + 1, B_PTREADY = B_SFULL + 2, B_DSREADY = B_SFULL + 3,
+            B_DSEMPTY = B_SFULL + 4, B_DQFULL = B_SFULL + 5, B_DQEMPTY = B_SFULL + 6,
+            B_ACC = B_SFULL + 7, B_DRAIN = B_SFULL + 8;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const float* stat_smem = reinterpret_cast<const float*>(smem + C::OFF_STAT);
@@ -183,13 +188,12 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       mbar_init(BAR(B_QEMPTY + s), 1);
     }
     mbar_init(BAR(B_SFULL), 1);
-    mbar_init(BAR(B_SCONS), 128);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(BAR(B_PREADY + b), 128);
-      mbar_init(BAR(B_PSEMPTY + b), 1);
-      mbar_init(BAR(B_DQFULL + b), 1);
-      mbar_init(BAR(B_DQEMPTY + b), 128);
-    }
+    mbar_init(BAR(B_DPFULL), 1);
+    mbar_init(BAR(B_PTREADY), 4);  // one arrival per softmax warp
+    mbar_init(BAR(B_DSREADY), 4);
+    mbar_init(BAR(B_DSEMPTY), 1);
+    mbar_init(BAR(B_DQFULL), 1);
+    mbar_init(BAR(B_DQEMPTY), 4);  // one arrival per dQ warp
     mbar_init(BAR(B_ACC), 1);
     mbar_init(BAR(B_DRAIN), 1);
     *abort_flag = 0;
@@ -208,10 +212,10 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       tma_prefetch_desc(&a.tmK);
       tma_prefetch_desc(&a.tmV);
       tma_prefetch_desc(&a.tmdO);
-      mbar_arrive_expect_tx(BAR(B_KV), 2 * C::KV_TILE);
+      mbar_arrive_expect_tx(BAR(B_KV), 2 * C::TILE);
       for (int c = 0; c < C::CH; ++c) {
-        tma_load_3d(sbase + C::OFF_K + c * C::KV_CHUNK, &a.tmK, BAR(B_KV), c * 64, k0, bh);
-        tma_load_3d(sbase + C::OFF_V + c * C::KV_CHUNK, &a.tmV, BAR(B_KV), c * 64, k0, bh);
+        tma_load_3d(sbase + C::OFF_K + c * C::ROW_CHUNK, &a.tmK, BAR(B_KV), c * 64, k0, bh);
+        tma_load_3d(sbase + C::OFF_V + c * C::ROW_CHUNK, &a.tmV, BAR(B_KV), c * 64, k0, bh);
       }
       int last[C::STAGES];
 #pragma unroll
@@ -221,11 +225,11 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         const int s = i % C::STAGES;
         const uint32_t ph = (i / C::STAGES) & 1;
         if (!mbar_wait(BAR(B_QEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(BAR(B_QFULL + s), 2 * C::Q_TILE + C::STAT_BYTES);
+        mbar_arrive_expect_tx(BAR(B_QFULL + s), 2 * C::TILE + C::STAT_BYTES);
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_3d(sbase + C::OFF_Q + s * C::Q_TILE + c * C::Q_CHUNK, &a.tmQ, BAR(B_QFULL + s),
+          tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
                       c * 64, i * C::BQ, bh);
-          tma_load_3d(sbase + C::OFF_DO + s * C::Q_TILE + c * C::Q_CHUNK, &a.tmdO,
+          tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
                       BAR(B_QFULL + s), c * 64, i * C::BQ, bh);
         }
         const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;
@@ -243,46 +247,54 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16_f32(128, C::BQ, false, false);   // S^T, dP^T
-      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);      // dV, dK
-      constexpr uint32_t id_dq = C::DQ_T ? idesc_bf16_f32(128, C::BQ, true, true)   // dQ^T = K^T dS^T
-                                         : idesc_bf16_f32(128, D, true, true);      // dQ = dS K
-      // S^T = K Q_i^T and dP^T = V dO_i^T  (A K-major [keys x d], B K-major [queries x d])
+      constexpr uint32_t id_s = idesc_bf16_f32(128, C::BQ, false, false);  // S^T, dP^T
+      constexpr uint32_t id_dv = idesc_bf16_f32(128, D, false, true);      // dV (A from TMEM)
+      constexpr uint32_t id_dk = idesc_bf16_f32(128, D, false, true);      // dK
+      constexpr uint32_t id_dq = C::DQ_T ? idesc_bf16_f32(128, C::BQ, true, true)  // dQ^T = K^T dS^T
+                                         : idesc_bf16_f32(128, D, true, true);    // dQ = dS K
+      // descriptors built once; K-steps only add byte offsets >> 4
+      const uint64_t dKk = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dKmn = sdesc_sw128(sbase + C::OFF_K, C::ROW_CHUNK, 1024);
+      const uint64_t dVk = sdesc_sw128(sbase + C::OFF_V, 16, 1024);
+      const uint64_t dQk = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dQmn = sdesc_sw128(sbase + C::OFF_Q, C::ROW_CHUNK, 1024);
+      const uint64_t dOk = sdesc_sw128(sbase + C::OFF_DO, 16, 1024);
+      const uint64_t dOmn = sdesc_sw128(sbase + C::OFF_DO, C::ROW_CHUNK, 1024);
+      const uint64_t dSk = sdesc_sw128(sbase + C::OFF_DS, 16, 1024);
+      const uint64_t dSmn = sdesc_sw128(sbase + C::OFF_DS, C::ROW_CHUNK, 1024);
+      const auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * C::ROW_CHUNK + (kk & 3) * 32) >> 4); };
+      const auto roff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };  // 16 rows of 128 B
+      const auto soff = [](int s) { return (uint64_t)((s * C::TILE) >> 4); };
+      // S^T = K Q_i^T, dP^T = V dO_i^T (K-dimension = d)
       auto issue_s = [&](int s) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offa = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          const uint32_t offb = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
-          mma_ss(tmem + C::COL_S, sdesc_sw128(sbase + C::OFF_K + offa, 16, 1024),
-                 sdesc_sw128(sbase + C::OFF_Q + s * C::Q_TILE + offb, 16, 1024), id_s, kk > 0);
-          mma_ss(tmem + C::COL_DP, sdesc_sw128(sbase + C::OFF_V + offa, 16, 1024),
-                 sdesc_sw128(sbase + C::OFF_DO + s * C::Q_TILE + offb, 16, 1024), id_s, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::COL_S, dKk + koff(kk), dQk + soff(s) + koff(kk), id_s, kk > 0);
       };
-      // dV += P^T dO_i, dK += dS^T Q_i  (A K-major [keys x queries], B MN-major [queries x d])
-      auto issue_acc = [&](int s, int b, bool acc) {
+      auto issue_dp = [&](int s) {
 #pragma unroll
-        for (int kk = 0; kk < C::BQ / 16; ++kk) {
-          const uint32_t offa = (kk >> 2) * C::PS_CHUNK + (kk & 3) * 32;
-          const uint32_t offb = kk * 2048;
-          mma_ss(tmem + C::COL_DV, sdesc_sw128(sbase + C::OFF_P + b * C::PS_TILE + offa, 16, 1024),
-                 sdesc_sw128(sbase + C::OFF_DO + s * C::Q_TILE + offb, C::Q_CHUNK, 1024), id_acc,
-                 (acc || kk > 0) ? 1u : 0u);
-          mma_ss(tmem + C::COL_DK, sdesc_sw128(sbase + C::OFF_DS + b * C::PS_TILE + offa, 16, 1024),
-                 sdesc_sw128(sbase + C::OFF_Q + s * C::Q_TILE + offb, C::Q_CHUNK, 1024), id_acc,
-                 (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::COL_DP, dVk + koff(kk), dOk + soff(s) + koff(kk), id_s, kk > 0);
       };
-      // dQ^T = K^T dS^T (d = 128) or dQ = dS K (d = 64); K-dimension = keys.
-      auto issue_dq = [&](int b, int bp) {
-        const uint32_t dcol = tmem + C::COL_DQ + b * C::DQC;
+      // dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i (K-dimension = queries)
+      auto issue_dv = [&](int s, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, dOmn + soff(s) + roff(kk), id_dv,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      auto issue_dk = [&](int s, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < C::BQ / 16; ++kk)
+          mma_ss(tmem + C::COL_DK, dSk + koff(kk), dQmn + soff(s) + roff(kk), id_dk,
+                 (acc || kk > 0) ? 1u : 0u);
+      };
+      // dQ_i (K-dimension = keys), into the dP^T columns; both operands MN-major
+      auto issue_dq = [&]() {
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
-          const uint32_t off = kk * 2048;
-          const uint64_t kd = sdesc_sw128(sbase + C::OFF_K + off, C::KV_CHUNK, 1024);
-          const uint64_t sd = sdesc_sw128(sbase + C::OFF_DS + bp * C::PS_TILE + off, C::PS_CHUNK, 1024);
-          if (C::DQ_T) mma_ss(dcol, kd, sd, id_dq, kk > 0);
-          else mma_ss(dcol, sd, kd, id_dq, kk > 0);
+          if (C::DQ_T) mma_ss(tmem + C::COL_DP, dKmn + roff(kk), dSmn + roff(kk), id_dq, kk > 0);
+          else mma_ss(tmem + C::COL_DP, dSmn + roff(kk), dKmn + roff(kk), id_dq, kk > 0);
         }
       };
       bool ok = mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns) &&
@@ -291,31 +303,38 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         tc_fence_after();
         issue_s(0);
         mma_commit(BAR(B_SFULL));
+        issue_dp(0);
+        mma_commit(BAR(B_DPFULL));
       }
       for (int i = 0; ok && i < n_q; ++i) {
         if (*abort_flag) { ok = false; break; }
         const int s = i % C::STAGES;
-        const int b = i & 1;                  // dQ TMEM buffer
-        const int bp = i % C::NPS;            // P^T/dS^T buffer
-        const uint32_t php = (i / C::NPS) & 1;
-        if (i + 1 < n_q) {
-          const int s1 = (i + 1) % C::STAGES;
-          const uint32_t ph1 = ((i + 1) / C::STAGES) & 1;
-          if (!mbar_wait(BAR(B_QFULL + s1), ph1, a.status, a.wait_limit_ns) ||
-              !mbar_wait(BAR(B_SCONS), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+        const bool more = i + 1 < n_q;
+        const int s1 = (i + 1) % C::STAGES;
+        const uint32_t ph1 = ((i + 1) / C::STAGES) & 1;
+        if (!mbar_wait(BAR(B_PTREADY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+        tc_fence_after();
+        issue_dv(s, i > 0);
+        if (more) {
+          if (!mbar_wait(BAR(B_QFULL + s1), ph1, a.status, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after();
-          issue_s(s1);
+          issue_s(s1);  // overwrites P^T(i): ordered after the dV products that read it
           mma_commit(BAR(B_SFULL));
         }
-        if (!mbar_wait(BAR(B_PREADY + bp), php, a.status, a.wait_limit_ns)) { ok = false; break; }
+        if (!mbar_wait(BAR(B_DSREADY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
         tc_fence_after();
-        issue_acc(s, bp, i > 0);
+        issue_dq();  // the dP^T columns: dP^T(i) was consumed before ds_ready
+        mma_commit(BAR(B_DQFULL));
+        issue_dk(s, i > 0);
         mma_commit(BAR(B_QEMPTY + s));  // Q_i, dO_i, stats: last use was dK/dV
-        if (!mbar_wait(BAR(B_DQEMPTY + b), ((i >> 1) & 1) ^ 1, a.status, a.wait_limit_ns)) { ok = false; break; }
-        tc_fence_after();
-        issue_dq(b, bp);
-        mma_commit(BAR(B_DQFULL + b));
-        mma_commit(BAR(B_PSEMPTY + bp));
+        mma_commit(BAR(B_DSEMPTY));     // dS^T(i): last use was dQ/dK
+        if (more) {
+          // dP^T(i+1) reuses the dQ columns once the dQ warps have read dQ(i)
+          if (!mbar_wait(BAR(B_DQEMPTY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp(s1);
+          mma_commit(BAR(B_DPFULL));
+        }
       }
       if (ok) mma_commit(BAR(B_ACC));
       else *abort_flag = 1;
@@ -330,72 +349,80 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
     const bool key_live = k0 + r < N;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const float c2 = a.scale_log2, scale = a.scale;
+    uint8_t* dsrow = smem + C::OFF_DS + r * 128;
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       const int s = i % C::STAGES;
-      const int b = i % C::NPS;
       bool w = mbar_wait(BAR(B_SFULL), i & 1, a.status, a.wait_limit_ns) &&
-               mbar_wait(BAR(B_QFULL + s), (i / C::STAGES) & 1, a.status, a.wait_limit_ns) &&
-               mbar_wait(BAR(B_PSEMPTY + b), ((i / C::NPS) & 1) ^ 1, a.status, a.wait_limit_ns);
+               mbar_wait(BAR(B_QFULL + s), (i / C::STAGES) & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       const float* lse2 = stat_smem + s * (C::STAT_BYTES / 4);
       const float* drow = lse2 + C::BQ;
-      uint8_t* pbuf = smem + C::OFF_P + b * C::PS_TILE;
-      uint8_t* dsbuf = smem + C::OFF_DS + b * C::PS_TILE;
+      // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, over the S^T
+      // columns; 32 query columns at a time
+      uint32_t pb[64];
 #pragma unroll
-      for (int h = 0; h < C::QCH; ++h) {
-        uint32_t sr[64], dr[64];
-        {
-          uint32_t t0[32], t1[32];
-          tmem_ld32(lane_addr + C::COL_S + 64 * h, t0);
-          tmem_ld32(lane_addr + C::COL_S + 64 * h + 32, t1);
-          tmem_ld_wait();
+      for (int h = 0; h < 4; ++h) {
+        uint32_t sr[32];
+        tmem_ld32(lane_addr + C::COL_S + 32 * h, sr);
+        tmem_ld_wait();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) { sr[k] = t0[k]; sr[32 + k] = t1[k]; }
-          tmem_ld32(lane_addr + C::COL_DP + 64 * h, t0);
-          tmem_ld32(lane_addr + C::COL_DP + 64 * h + 32, t1);
-          tmem_ld_wait();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) { dr[k] = t0[k]; dr[32 + k] = t1[k]; }
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + 32 * h + 4 * k4);
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 0]), c2, -l4.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 1]), c2, -l4.y));
+          float p2 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 2]), c2, -l4.z));
+          float p3 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 3]), c2, -l4.w));
+          if (!key_live) p0 = p1 = p2 = p3 = 0.f;
+          pb[16 * h + 2 * k4] = pack_bf16x2(p0, p1);
+          pb[16 * h + 2 * k4 + 1] = pack_bf16x2(p2, p3);
         }
-        if (h == C::QCH - 1) {
-          tc_fence_before();
-          mbar_arrive(BAR(B_SCONS));
+      }
+      tmem_st32(lane_addr + C::COL_S, *reinterpret_cast<uint32_t(*)[32]>(&pb[0]));
+      tmem_st32(lane_addr + C::COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&pb[32]));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_PTREADY));
+      // phase 2: dS^T = P^T o (dP^T - D) * scale, bf16, into the swizzled dS^T
+      // tile ([128 keys][64 queries] chunks; 16-byte unit c of row r lands at
+      // unit c ^ (r & 7)); 32 query columns at a time
+      w = mbar_wait(BAR(B_DPFULL), i & 1, a.status, a.wait_limit_ns) &&
+          mbar_wait(BAR(B_DSEMPTY), (i & 1) ^ 1, a.status, a.wait_limit_ns);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        uint32_t dr[32];
+        tmem_ld32(lane_addr + C::COL_DP + 32 * h, dr);
+        tmem_ld_wait();
+        uint32_t dk[16];
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(drow + 32 * h + 4 * k4);
+          const float2 pa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[16 * h + 2 * k4]));
+          const float2 pc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[16 * h + 2 * k4 + 1]));
+          const float g0 = pa.x * (__uint_as_float(dr[4 * k4 + 0]) - d4.x) * scale;
+          const float g1 = pa.y * (__uint_as_float(dr[4 * k4 + 1]) - d4.y) * scale;
+          const float g2 = pc.x * (__uint_as_float(dr[4 * k4 + 2]) - d4.z) * scale;
+          const float g3 = pc.y * (__uint_as_float(dr[4 * k4 + 3]) - d4.w) * scale;
+          dk[2 * k4] = pack_bf16x2(g0, g1);
+          dk[2 * k4 + 1] = pack_bf16x2(g2, g3);
         }
-        uint32_t pk[32], dk[32];
+        uint8_t* chunk_row = dsrow + (h >> 1) * C::ROW_CHUNK;
 #pragma unroll
-        for (int k4 = 0; k4 < 16; ++k4) {
-          const int q = 64 * h + 4 * k4;
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + q);
-          const float4 d4 = *reinterpret_cast<const float4*>(drow + q);
-          const float lq[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dq[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            p[u] = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + u]), c2, -lq[u]));
-            ds[u] = p[u] * (__uint_as_float(dr[4 * k4 + u]) - dq[u]) * scale;
-            if (!key_live) p[u] = ds[u] = 0.f;
-          }
-          pk[2 * k4] = pack_bf16x2(p[0], p[1]);
-          pk[2 * k4 + 1] = pack_bf16x2(p[2], p[3]);
-          dk[2 * k4] = pack_bf16x2(ds[0], ds[1]);
-          dk[2 * k4 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
-        // row r of a 128-byte-swizzled [128 x 64] bf16 tile: 16-byte chunk c at c ^ (r & 7)
-        uint8_t* prow = pbuf + h * C::PS_CHUNK + r * 128;
-        uint8_t* drow_s = dsbuf + h * C::PS_CHUNK + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int pc = (c ^ (r & 7)) * 16;
-          *reinterpret_cast<uint4*>(prow + pc) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(drow_s + pc) = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        for (int u = 0; u < 4; ++u) {
+          const int c = (h & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(chunk_row + ((c ^ (r & 7)) * 16)) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(BAR(B_PREADY + b));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_DSREADY));
     }
     if (ok) {
       const bool w = mbar_wait(BAR(B_ACC), 0, a.status, a.wait_limit_ns);
@@ -432,34 +459,32 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
     const int wq = warp & 3;
     const int t = wq * 32 + lane;  // TMEM lane: d index (dQ^T) or query row (dQ)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    constexpr int NCOL = C::DQ_T ? C::BQ : D;  // columns of the dQ tile
     for (int i = 0; i < n_q; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int b = i & 1;
-      const bool w = mbar_wait(BAR(B_DQFULL + b), (i >> 1) & 1, a.status, a.wait_limit_ns);
+      const bool w = mbar_wait(BAR(B_DQFULL), i & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { *abort_flag = 1; break; }
       tc_fence_after();
-      uint32_t v[64];
-      {
-        uint32_t t0[32], t1[32];
-        tmem_ld32(lane_addr + C::COL_DQ + b * C::DQC, t0);
-        tmem_ld32(lane_addr + C::COL_DQ + b * C::DQC + 32, t1);
-        tmem_ld_wait();
+      uint32_t v[NCOL];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) { v[k] = t0[k]; v[32 + k] = t1[k]; }
-      }
+      for (int q = 0; q < NCOL / 32; ++q)
+        tmem_ld32(lane_addr + C::COL_DP + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * q]));
+      tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(BAR(B_DQEMPTY + b));
-      const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_DQEMPTY));
+      const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;  // padded rows are scratch
       if (C::DQ_T) {
-        // lane t holds dQ[row0 + q][t] for q = 0..63: warp-coalesced 128-byte reductions
+        // lane t holds dQ[row0 + q][t] for every query q: each warp instruction
+        // adds one contiguous 128-byte segment of a dQ row
         float* base = a.dQacc + row0 * D + t;
 #pragma unroll
-        for (int q = 0; q < 64; ++q) atomicAdd(base + (size_t)q * D, __uint_as_float(v[q]));
+        for (int q = 0; q < NCOL; ++q) atomicAdd(base + (size_t)q * D, __uint_as_float(v[q]));
       } else {
-        // lane t holds the whole dQ row (64 values) of query row0 + t
+        // lane t holds the whole dQ row of query row0 + t
         float4* base = reinterpret_cast<float4*>(a.dQacc + (row0 + t) * D);
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
+        for (int q = 0; q < D / 4; ++q)
           atomicAdd(base + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
       }
@@ -477,7 +502,6 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t st) {
   using C = BwdCfg<D>;
-  static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
   cudaError_t e = cudaSuccess;
   if (stages & kStagePre) {
     constexpr int RPW = 32 / (D / 8);

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
     }
     for (int t = 0; t < C::QT; ++t) {
       mbar_init(BAR(B_SFULL + t), 1);
-      mbar_init(BAR(B_PFULL + t), 128);
+      mbar_init(BAR(B_PFULL + t), 4);  // one arrival per softmax warp
       mbar_init(BAR(B_ODONE + t), 1);
     }
     mbar_init(BAR(B_DRAIN), 1);
@@ -162,23 +162,29 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      // Descriptors are built once; advancing along K only adds a byte offset
+      // (>> 4) to the 14-bit start-address field, which cannot carry out of it
+      // because every operand lies below 256 KB of shared memory.
+      const uint64_t dQ0 = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
       auto issue_s = [&](int t, int s) {
+        const uint64_t qa = dQ0 + (uint64_t)((t * C::TILE_BYTES) >> 4);
+        const uint64_t kb = dK0 + (uint64_t)((s * C::TILE_BYTES) >> 4);
+        const uint32_t dcol = tmem + C::S_COL(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sbase + C::OFF_Q + t * C::TILE_BYTES + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sbase + C::OFF_K + s * C::TILE_BYTES + off, 16, 1024);
-          mma_ss(tmem + C::S_COL(t), ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+          mma_ss(dcol, qa + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
+        const uint64_t vb = dV0 + (uint64_t)((s * C::TILE_BYTES) >> 4);
+        const uint32_t dcol = tmem + C::O_COL(t), acol = tmem + C::S_COL(t);
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          const uint64_t bd =
-              sdesc_sw128(sbase + C::OFF_V + s * C::TILE_BYTES + kk * 2048, C::CHUNK_BYTES, 1024);
-          mma_ts(tmem + C::O_COL(t), tmem + C::S_COL(t) + kk * 8, bd, idesc_o,
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ts(dcol, acol + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_o,
                  (acc || kk > 0) ? 1u : 0u);
-        }
       };
       bool ok = mbar_wait(BAR(B_QFULL), 0, a.status, a.wait_limit_ns);
       ok = ok && mbar_wait(BAR(B_KFULL + 0), 0, a.status, a.wait_limit_ns);
@@ -289,12 +295,10 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
       l = l * alpha + sum;
       m_ref = m_new;
+      // P V of the previous tile is complete here: S of this tile was
+      // committed after it, and a commit tracks every earlier MMA. So O can be
+      // rescaled without waiting on o_done (only the epilogue waits on it).
       if (j > 0) {
-        // P V of the previous tile must be complete before O is touched and
-        // before this tile's P is released.
-        w = mbar_wait(BAR(B_ODONE + t), (j - 1) & 1, a.status, a.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        tc_fence_after();
         if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
@@ -309,7 +313,8 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(BAR(B_PFULL + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_PFULL + t));
     }
     tmem_st_wait();  // no TMEM store may be in flight when the loop is left early
     if (ok && n_kv > 0) {

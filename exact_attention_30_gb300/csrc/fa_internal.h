@@ -62,7 +62,7 @@ cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cu
 constexpr int kBwdRowPad = 128;
 // Query rows per streamed tile of the bf16 backward kernel (its Q/dO TMA box
 // height); must match BwdCfg<d>::BQ.
-constexpr int bwd_query_tile(int d) { return d == 128 ? 64 : 128; }
+constexpr int bwd_query_tile(int d) { return d > 0 ? 128 : 128; }
 
 // Bounded-wait probe (fa_debug_timeout_probe).
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
