@@ -10,9 +10,9 @@
 // sum over the full row is available before any tile is visited.
 //
 // Three kernels on the caller's stream:
-//  1. bwd_pre:   D and LSE*log2(e) per row into the workspace (rows padded to
-//                a multiple of 128: D = 0, LSE*log2(e) = +inf past N, which
-//                makes P = 0 there), and zero the fp32 dQ accumulator.
+//  1. bwd_pre:   -D and -LSE*log2(e) per row into the workspace (rows
+//                padded to a multiple of 128: 0 and -inf past N, which makes
+//                P = 0 there), and zero the fp32 dQ accumulator.
 //  2. bwd_main:  one CTA per (batch*head, 128-key tile j); K_j, V_j stay in
 //                shared memory while 128-query tiles i stream through a TMA
 //                ring. All products run on tcgen05 with fp32 accumulators in
@@ -29,7 +29,7 @@
 //                it to the accumulator with 16-byte atomics. Per query tile the
 //                MMA order is dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1), so the
 //                next tile's recompute overlaps this tile's softmax.
-//  3. dq_convert: fp32 accumulator -> bf16 dQ.
+//  3. dq_convert: fp32 accumulator times scale -> bf16 dQ.
 // TMEM (512 columns): S^T|P^T, dP^T|dQ, dV, dK.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -81,9 +81,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, int BH) {
   }
 #pragma unroll
   for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  // Stored negated so that the main kernel forms P = 2^(s*c - LSE*log2e) with
+  // one fused multiply-add and dP - D with one add (exact when they are equal).
   if (prow < total && l == 0) {
-    a.Drow[prow] = live ? acc : 0.f;
-    a.lse2[prow] = live ? a.LSE[(size_t)bh * a.N + (size_t)n] * 1.4426950408889634f : INFINITY;
+    a.Drow[prow] = live ? -acc : 0.f;
+    a.lse2[prow] = live ? -a.LSE[(size_t)bh * a.N + (size_t)n] * 1.4426950408889634f : -INFINITY;
   }
 }
 
@@ -101,10 +103,11 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, int BH
   const float4* src = reinterpret_cast<const float4*>(a.dQacc + ((size_t)bh * a.Npad + n) * D + g * 8);
   const float4 x = src[0], y = src[1];
   uint4 u;
-  u.x = pack_bf16x2(x.x, x.y);
-  u.y = pack_bf16x2(x.z, x.w);
-  u.z = pack_bf16x2(y.x, y.y);
-  u.w = pack_bf16x2(y.z, y.w);
+  const float f = a.scale;  // the softmax scale of dS, applied once here
+  u.x = pack_bf16x2(f * x.x, f * x.y);
+  u.y = pack_bf16x2(f * x.z, f * x.w);
+  u.z = pack_bf16x2(f * y.x, f * y.y);
+  u.w = pack_bf16x2(f * y.z, f * y.w);
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dQ) + (size_t)row * D + g * 8) = u;
 }
 
@@ -120,7 +123,13 @@ struct BwdCfg {
   // dQ = dS K (queries on the lanes; an M = 64 product would be needed otherwise)
   static constexpr bool DQ_T = (D == 128);
   static constexpr int CH = D / 64;                  // 128-byte chunks per K/V/Q/dO row
-  static constexpr int STAGES = (D == 128) ? 2 : 3;  // Q/dO ring depth
+  // Q_i (with its LSE/D statistics) is read by S^T(i), issued one tile
+  // early, and last by dK(i); dO_i by dP^T(i), also issued one tile early,
+  // and last by dV(i), the first product of tile i. So Q needs a deep ring
+  // for its loads to run ahead, while one dO slot already gives its load
+  // most of a tile of lead time.
+  static constexpr int QSTAGES = (D == 128) ? 3 : 4;
+  static constexpr int DOSTAGES = (D == 128) ? 1 : 2;
   static constexpr int ROW_CHUNK = 128 * 128;        // 128 rows x 128 bytes, swizzled
   static constexpr int TILE = CH * ROW_CHUNK;        // 128 rows x D bf16
   static constexpr int DS_TILE = 2 * ROW_CHUNK;      // dS^T: [128 keys][128 queries] bf16
@@ -129,12 +138,14 @@ struct BwdCfg {
   static constexpr int OFF_V = OFF_K + TILE;
   static constexpr int OFF_DS = OFF_V + TILE;
   static constexpr int OFF_Q = OFF_DS + DS_TILE;
-  static constexpr int OFF_DO = OFF_Q + STAGES * TILE;
-  static constexpr int OFF_STAT = OFF_DO + STAGES * TILE;
-  static constexpr int OFF_BAR = OFF_STAT + STAGES * STAT_BYTES;
-  // barriers: kv_full, q_full[S], q_empty[S], s_full, dp_full, pt_ready, ds_ready,
-  //           ds_empty, dq_full, dq_empty, acc_done, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 9;
+  static constexpr int OFF_DO = OFF_Q + QSTAGES * TILE;
+  static constexpr int OFF_STAT = OFF_DO + DOSTAGES * TILE;
+  static constexpr int STATSTAGES = 2;  // LSE*log2e and D, read by both softmax phases
+  static constexpr int OFF_BAR = OFF_STAT + STATSTAGES * STAT_BYTES;
+  // barriers: kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], st_full[2],
+  //           st_empty[2], s_full, dp_full, pt_ready, ds_ready, ds_empty, dq_full,
+  //           dq_empty, acc_done, drain
+  static constexpr int NBAR = 1 + 2 * QSTAGES + 2 * DOSTAGES + 2 * STATSTAGES + 9;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_MAX = 227 * 1024;
   // request 1 KB of alignment slack when it fits; the kernel checks alignment
@@ -167,7 +178,9 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
   }
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  const int B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + C::STAGES, B_SFULL = 1 + 2 * C::STAGES,
+  const int B_KV = 0, B_QFULL = 1, B_QEMPTY = 1 + C::QSTAGES, B_DOFULL = 1 + 2 * C::QSTAGES,
+            B_DOEMPTY = B_DOFULL + C::DOSTAGES, B_STFULL = B_DOEMPTY + C::DOSTAGES,
+            B_STEMPTY = B_STFULL + C::STATSTAGES, B_SFULL = B_STEMPTY + C::STATSTAGES,
             B_DPFULL = B_SFULL + 1, B_PTREADY = B_SFULL + 2, B_DSREADY = B_SFULL + 3,
             B_DSEMPTY = B_SFULL + 4, B_DQFULL = B_SFULL + 5, B_DQEMPTY = B_SFULL + 6,
             B_ACC = B_SFULL + 7, B_DRAIN = B_SFULL + 8;
@@ -183,9 +196,17 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_KV), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < C::QSTAGES; ++s) {
       mbar_init(BAR(B_QFULL + s), 1);
       mbar_init(BAR(B_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::DOSTAGES; ++s) {
+      mbar_init(BAR(B_DOFULL + s), 1);
+      mbar_init(BAR(B_DOEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::STATSTAGES; ++s) {
+      mbar_init(BAR(B_STFULL + s), 1);
+      mbar_init(BAR(B_STEMPTY + s), 4);  // one arrival per softmax warp
     }
     mbar_init(BAR(B_SFULL), 1);
     mbar_init(BAR(B_DPFULL), 1);
@@ -206,42 +227,74 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer: K, V, Q ring
     if (lane == 0) {
       tma_prefetch_desc(&a.tmQ);
       tma_prefetch_desc(&a.tmK);
       tma_prefetch_desc(&a.tmV);
-      tma_prefetch_desc(&a.tmdO);
       mbar_arrive_expect_tx(BAR(B_KV), 2 * C::TILE);
       for (int c = 0; c < C::CH; ++c) {
         tma_load_3d(sbase + C::OFF_K + c * C::ROW_CHUNK, &a.tmK, BAR(B_KV), c * 64, k0, bh);
         tma_load_3d(sbase + C::OFF_V + c * C::ROW_CHUNK, &a.tmV, BAR(B_KV), c * 64, k0, bh);
       }
-      int last[C::STAGES];
+      int last[C::QSTAGES];
 #pragma unroll
-      for (int s = 0; s < C::STAGES; ++s) last[s] = -1;
+      for (int s = 0; s < C::QSTAGES; ++s) last[s] = -1;
       for (int i = 0; i < n_q; ++i) {
         if (*abort_flag) break;
-        const int s = i % C::STAGES;
-        const uint32_t ph = (i / C::STAGES) & 1;
+        const int s = i % C::QSTAGES;
+        const uint32_t ph = (i / C::QSTAGES) & 1;
         if (!mbar_wait(BAR(B_QEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(BAR(B_QFULL + s), 2 * C::TILE + C::STAT_BYTES);
-        for (int c = 0; c < C::CH; ++c) {
+        mbar_arrive_expect_tx(BAR(B_QFULL + s), C::TILE);
+        for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
                       c * 64, i * C::BQ, bh);
-          tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
-                      BAR(B_QFULL + s), c * 64, i * C::BQ, bh);
-        }
-        const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;
-        bulk_load(sbase + C::OFF_STAT + s * C::STAT_BYTES, a.lse2 + row0, C::BQ * 4, BAR(B_QFULL + s));
-        bulk_load(sbase + C::OFF_STAT + s * C::STAT_BYTES + C::BQ * 4, a.Drow + row0, C::BQ * 4,
-                  BAR(B_QFULL + s));
         last[s] = i;
       }
       mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns);
 #pragma unroll
-      for (int s = 0; s < C::STAGES; ++s)
-        if (last[s] >= 0) mbar_wait(BAR(B_QFULL + s), (last[s] / C::STAGES) & 1, a.status, a.wait_limit_ns);
+      for (int s = 0; s < C::QSTAGES; ++s)
+        if (last[s] >= 0) mbar_wait(BAR(B_QFULL + s), (last[s] / C::QSTAGES) & 1, a.status, a.wait_limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ producer: stats, dO ring
+    if (lane == 0) {
+      tma_prefetch_desc(&a.tmdO);
+      int last[C::DOSTAGES], last_st[C::STATSTAGES];
+#pragma unroll
+      for (int s = 0; s < C::DOSTAGES; ++s) last[s] = -1;
+#pragma unroll
+      for (int s = 0; s < C::STATSTAGES; ++s) last_st[s] = -1;
+      for (int i = 0; i < n_q; ++i) {
+        if (*abort_flag) break;
+        {
+          const int t = i % C::STATSTAGES;
+          const uint32_t pt = (i / C::STATSTAGES) & 1;
+          if (!mbar_wait(BAR(B_STEMPTY + t), pt ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
+          mbar_arrive_expect_tx(BAR(B_STFULL + t), C::STAT_BYTES);
+          const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;
+          bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES, a.lse2 + row0, C::BQ * 4, BAR(B_STFULL + t));
+          bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES + C::BQ * 4, a.Drow + row0, C::BQ * 4,
+                    BAR(B_STFULL + t));
+          last_st[t] = i;
+        }
+        const int s = i % C::DOSTAGES;
+        const uint32_t ph = (i / C::DOSTAGES) & 1;
+        if (!mbar_wait(BAR(B_DOEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(BAR(B_DOFULL + s), C::TILE);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
+                      BAR(B_DOFULL + s), c * 64, i * C::BQ, bh);
+        last[s] = i;
+      }
+#pragma unroll
+      for (int s = 0; s < C::DOSTAGES; ++s)
+        if (last[s] >= 0) mbar_wait(BAR(B_DOFULL + s), (last[s] / C::DOSTAGES) & 1, a.status, a.wait_limit_ns);
+#pragma unroll
+      for (int s = 0; s < C::STATSTAGES; ++s)
+        if (last_st[s] >= 0)
+          mbar_wait(BAR(B_STFULL + s), (last_st[s] / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -264,7 +317,7 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       const uint64_t dSmn = sdesc_sw128(sbase + C::OFF_DS, C::ROW_CHUNK, 1024);
       const auto koff = [](int kk) { return (uint64_t)(((kk >> 2) * C::ROW_CHUNK + (kk & 3) * 32) >> 4); };
       const auto roff = [](int kk) { return (uint64_t)((kk * 2048) >> 4); };  // 16 rows of 128 B
-      const auto soff = [](int s) { return (uint64_t)((s * C::TILE) >> 4); };
+      const auto soff = [](int s) { return (uint64_t)((s * C::TILE) >> 4); };  // ring slot s
       // S^T = K Q_i^T, dP^T = V dO_i^T (K-dimension = d)
       auto issue_s = [&](int s) {
 #pragma unroll
@@ -298,23 +351,25 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         }
       };
       bool ok = mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns) &&
-                mbar_wait(BAR(B_QFULL + 0), 0, a.status, a.wait_limit_ns);
+                mbar_wait(BAR(B_QFULL + 0), 0, a.status, a.wait_limit_ns) &&
+                mbar_wait(BAR(B_DOFULL + 0), 0, a.status, a.wait_limit_ns);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         mma_commit(BAR(B_SFULL));
-        issue_dp(0);
+        issue_dp(0);  // dO ring slot 0
         mma_commit(BAR(B_DPFULL));
       }
       for (int i = 0; ok && i < n_q; ++i) {
         if (*abort_flag) { ok = false; break; }
-        const int s = i % C::STAGES;
+        const int s = i % C::QSTAGES, so = i % C::DOSTAGES;
         const bool more = i + 1 < n_q;
-        const int s1 = (i + 1) % C::STAGES;
-        const uint32_t ph1 = ((i + 1) / C::STAGES) & 1;
+        const int s1 = (i + 1) % C::QSTAGES, so1 = (i + 1) % C::DOSTAGES;
+        const uint32_t ph1 = ((i + 1) / C::QSTAGES) & 1, pho1 = ((i + 1) / C::DOSTAGES) & 1;
         if (!mbar_wait(BAR(B_PTREADY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
         tc_fence_after();
-        issue_dv(s, i > 0);
+        issue_dv(so, i > 0);
+        mma_commit(BAR(B_DOEMPTY + so));  // dO_i: last use was dV
         if (more) {
           if (!mbar_wait(BAR(B_QFULL + s1), ph1, a.status, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after();
@@ -326,13 +381,14 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         issue_dq();  // the dP^T columns: dP^T(i) was consumed before ds_ready
         mma_commit(BAR(B_DQFULL));
         issue_dk(s, i > 0);
-        mma_commit(BAR(B_QEMPTY + s));  // Q_i, dO_i, stats: last use was dK/dV
+        mma_commit(BAR(B_QEMPTY + s));  // Q_i: last use was dK
         mma_commit(BAR(B_DSEMPTY));     // dS^T(i): last use was dQ/dK
         if (more) {
           // dP^T(i+1) reuses the dQ columns once the dQ warps have read dQ(i)
-          if (!mbar_wait(BAR(B_DQEMPTY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+          if (!mbar_wait(BAR(B_DQEMPTY), i & 1, a.status, a.wait_limit_ns) ||
+              !mbar_wait(BAR(B_DOFULL + so1), pho1, a.status, a.wait_limit_ns)) { ok = false; break; }
           tc_fence_after();
-          issue_dp(s1);
+          issue_dp(so1);
           mma_commit(BAR(B_DPFULL));
         }
       }
@@ -348,20 +404,21 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
     const int r = wq * 32 + lane;  // key row within the tile == TMEM lane
     const bool key_live = k0 + r < N;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
-    const float c2 = a.scale_log2, scale = a.scale;
+    const uint64_t c22 = f2_pack(a.scale_log2, a.scale_log2);
+    const float scale = a.scale;
     uint8_t* dsrow = smem + C::OFF_DS + r * 128;
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-      const int s = i % C::STAGES;
+      const int st = i % C::STATSTAGES;
       bool w = mbar_wait(BAR(B_SFULL), i & 1, a.status, a.wait_limit_ns) &&
-               mbar_wait(BAR(B_QFULL + s), (i / C::STAGES) & 1, a.status, a.wait_limit_ns);
+               mbar_wait(BAR(B_STFULL + st), (i / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      const float* lse2 = stat_smem + s * (C::STAT_BYTES / 4);
+      const float* lse2 = stat_smem + st * (C::STAT_BYTES / 4);
       const float* drow = lse2 + C::BQ;
       // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, over the S^T
-      // columns; 32 query columns at a time
+      // columns; 32 query columns at a time, pairs in packed fp32 arithmetic
       uint32_t pb[64];
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
@@ -370,11 +427,11 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         tmem_ld_wait();
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + 32 * h + 4 * k4);
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 0]), c2, -l4.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 1]), c2, -l4.y));
-          float p2 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 2]), c2, -l4.z));
-          float p3 = ex2_approx(fmaf(__uint_as_float(sr[4 * k4 + 3]), c2, -l4.w));
+          // nl = -LSE*log2e of four query columns
+          const float4 nl = *reinterpret_cast<const float4*>(lse2 + 32 * h + 4 * k4);
+          const float2 xa = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4]), __uint_as_float(sr[4 * k4 + 1])), c22, f2_pack(nl.x, nl.y)));
+          const float2 xb = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4 + 2]), __uint_as_float(sr[4 * k4 + 3])), c22, f2_pack(nl.z, nl.w)));
+          float p0 = ex2_approx(xa.x), p1 = ex2_approx(xa.y), p2 = ex2_approx(xb.x), p3 = ex2_approx(xb.y);
           if (!key_live) p0 = p1 = p2 = p3 = 0.f;
           pb[16 * h + 2 * k4] = pack_bf16x2(p0, p1);
           pb[16 * h + 2 * k4 + 1] = pack_bf16x2(p2, p3);
@@ -401,15 +458,17 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
         uint32_t dk[16];
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(drow + 32 * h + 4 * k4);
+          // nd = -D of four query columns; dS' = P * (dP - D). The softmax
+          // scale of dS is applied once to dK (epilogue) and dQ (convert).
+          const float4 nd = *reinterpret_cast<const float4*>(drow + 32 * h + 4 * k4);
           const float2 pa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[16 * h + 2 * k4]));
           const float2 pc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[16 * h + 2 * k4 + 1]));
-          const float g0 = pa.x * (__uint_as_float(dr[4 * k4 + 0]) - d4.x) * scale;
-          const float g1 = pa.y * (__uint_as_float(dr[4 * k4 + 1]) - d4.y) * scale;
-          const float g2 = pc.x * (__uint_as_float(dr[4 * k4 + 2]) - d4.z) * scale;
-          const float g3 = pc.y * (__uint_as_float(dr[4 * k4 + 3]) - d4.w) * scale;
-          dk[2 * k4] = pack_bf16x2(g0, g1);
-          dk[2 * k4 + 1] = pack_bf16x2(g2, g3);
+          const uint64_t ta = fadd2(f2_pack(__uint_as_float(dr[4 * k4]), __uint_as_float(dr[4 * k4 + 1])), f2_pack(nd.x, nd.y));
+          const uint64_t tb = fadd2(f2_pack(__uint_as_float(dr[4 * k4 + 2]), __uint_as_float(dr[4 * k4 + 3])), f2_pack(nd.z, nd.w));
+          const float2 ga = f2_unpack(fmul2(f2_pack(pa.x, pa.y), ta));
+          const float2 gb = f2_unpack(fmul2(f2_pack(pc.x, pc.y), tb));
+          dk[2 * k4] = pack_bf16x2(ga.x, ga.y);
+          dk[2 * k4 + 1] = pack_bf16x2(gb.x, gb.y);
         }
         uint8_t* chunk_row = dsrow + (h >> 1) * C::ROW_CHUNK;
 #pragma unroll
@@ -422,7 +481,10 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_DSREADY));
+      if (lane == 0) {
+        mbar_arrive(BAR(B_DSREADY));
+        mbar_arrive(BAR(B_STEMPTY + st));  // this tile's LSE/D are no longer read
+      }
     }
     if (ok) {
       const bool w = mbar_wait(BAR(B_ACC), 0, a.status, a.wait_limit_ns);
@@ -436,6 +498,7 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
+        const float f = which == 0 ? 1.f : scale;  // dK carries the softmax scale of dS
         __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? a.dV : a.dK) + out_row;
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) {
@@ -446,10 +509,10 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              d4[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]), __uint_as_float(v[8 * u + 1])),
-                                 pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                                 pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                                 pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+              d4[u] = make_uint4(pack_bf16x2(f * __uint_as_float(v[8 * u]), f * __uint_as_float(v[8 * u + 1])),
+                                 pack_bf16x2(f * __uint_as_float(v[8 * u + 2]), f * __uint_as_float(v[8 * u + 3])),
+                                 pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
+                                 pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
           }
         }
       }

@@ -246,60 +246,86 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       bool w = mbar_wait(BAR(B_SFULL + t), j & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      // raw scores of this row: four 32-column loads, one wait
-      uint32_t r[128];
-      tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-      tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
-      tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
-      tmem_ld_wait();
+      // Raw scores of this row, 64 columns at a time (two 32-column loads, one
+      // wait); columns past N read as -inf.
+      uint32_t r[64];
       const int valid = N - j * C::BN;
-      if (valid < C::BN) {
+      auto load_half = [&](int h) {
+        tmem_ld32(s_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(s_addr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld_wait();
+        if (valid < C::BN) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= valid) r[i] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 64; ++i)
+            if (64 * h + i >= valid) r[i] = __float_as_uint(-INFINITY);
+        }
+      };
+      // Speculative pass: exponentiate against the current reference max while
+      // this tile's row max is computed alongside (max, exp2 and the sums run
+      // on different pipes). Only when the tile max exceeds the reference by
+      // more than kRescaleLog2 -- always on the first tile, rarely later -- is
+      // the tile redone against the new max, from S re-read out of TMEM (P is
+      // written over S only after this decision). Scale > 0 commutes with max.
+      // Pairs of columns go through packed fp32 arithmetic (fma/add .f32x2)
+      // and a three-input max: fewer issued instructions per score, which
+      // also leaves issue slots to the MMA warp sharing these sub-partitions.
+      float mx[4];
+      uint64_t sm2[4];
+      uint32_t pk[64];
+      const uint64_t c22 = f2_pack(c2, c2);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) { mx[u] = -INFINITY; sm2[u] = 0ull; }
+      {
+        const float neg_m = (j > 0) ? -m_ref : 0.f;
+        const uint64_t nm2 = f2_pack(neg_m, neg_m);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          load_half(h);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+            mx[i & 3] = fmax3(mx[i & 3], s0, s1);
+            const float2 x = f2_unpack(ffma2(f2_pack(s0, s1), c22, nm2));
+            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
+            pk[32 * h + i] = pack_bf16x2(p0, p1);
+          }
+        }
       }
-      // row max with 8 independent chains (scale > 0 commutes with max)
-      float mx[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(r[u]);
-#pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(r[i]));
-#pragma unroll
-      for (int u = 0; u < 4; ++u) mx[u] = fmaxf(mx[u], mx[u + 4]);
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
       const bool need = mt > m_ref + kRescaleLog2;
-      const float m_new = need ? mt : m_ref;
-      const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-      const float neg_m = -m_new;
-      // p = 2^(s*c2 - m_new), summed with 8 independent chains, rounded to
-      // bf16 and written over the first 64 S columns in two 32-column halves
-      // (S of this tile is already in registers).
-      float sm8[8];
+      float alpha = 1.f;
+      if (__any_sync(0xffffffffu, need)) {
+        // redo for the whole warp (rows that keep their max recompute the
+        // same values)
+        const float m_new = need ? mt : m_ref;
+        alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+        const uint64_t nm2 = f2_pack(-m_new, -m_new);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) sm8[u] = 0.f;
+        for (int u = 0; u < 4; ++u) sm2[u] = 0ull;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
+        for (int h = 0; h < 2; ++h) {
+          load_half(h);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = 64 * hh + 2 * i;
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c]), c2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c + 1]), c2, neg_m));
-          sm8[c & 7] += p0;
-          sm8[(c + 1) & 7] += p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 32; ++i) {
+            const float2 x = f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c22, nm2));
+            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+            sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
+            pk[32 * h + i] = pack_bf16x2(p0, p1);
+          }
         }
-        tmem_st32(s_addr + 32 * hh, pk);
+        m_ref = m_new;
       }
-      const float sum = ((sm8[0] + sm8[1]) + (sm8[2] + sm8[3])) + ((sm8[4] + sm8[5]) + (sm8[6] + sm8[7]));
-      l = l * alpha + sum;
-      m_ref = m_new;
+      // P (bf16) over the first 64 S columns
+      tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      const float2 sa = f2_unpack(fadd2(fadd2(sm2[0], sm2[1]), fadd2(sm2[2], sm2[3])));
+      l = l * alpha + (sa.x + sa.y);
       // P V of the previous tile is complete here: S of this tile was
       // committed after it, and a commit tracks every earlier MMA. So O can be
       // rescaled without waiting on o_done (only the epilogue waits on it).
       if (j > 0) {
-        if (__any_sync(0xffffffffu, need)) {
+        if (__any_sync(0xffffffffu, need)) {  // alpha == 1 on rows whose max did not move
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];

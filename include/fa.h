@@ -68,8 +68,8 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 /*
  * Bytes of device scratch that fa_bwd needs for this problem (0 on invalid
  * arguments). The caller allocates it; its contents on entry do not matter.
- * Holds the fp32 dQ accumulator and the per-row D = rowsum(dO o O) and
- * LSE * log2(e) statistics.
+ * Holds the fp32 dQ accumulator and per-row statistics derived from
+ * D = rowsum(dO o O) and the LSE.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt);
 
@@ -93,12 +93,14 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 /*
  * One stage of fa_bwd, for callers that schedule or time the stages
  * separately. Same arguments and validation as fa_bwd, plus `stage`:
- *   FA_BWD_PREPROCESS (0): D = rowsum(dO o O) and LSE * log2(e) per row into
- *                          the workspace; zero the workspace's dQ accumulator.
+ *   FA_BWD_PREPROCESS (0): per-row statistics from D = rowsum(dO o O) and
+ *                          the LSE into the workspace; zero the workspace's
+ *                          dQ accumulator.
  *   FA_BWD_MAIN       (1): recompute P tile by tile; write dK, dV; add dQ
- *                          into the workspace accumulator. Needs stage 0 done.
- *   FA_BWD_DQ_CONVERT (2): workspace dQ accumulator -> dQ in dtype `dt`.
- *                          Needs stage 1 done.
+ *                          into the workspace accumulator (for bf16 without
+ *                          the softmax scale). Needs stage 0 done.
+ *   FA_BWD_DQ_CONVERT (2): workspace dQ accumulator -> dQ in dtype `dt`
+ *                          (bf16: the scale is applied here). Needs stage 1.
  * Stages run in that order on one workspace; fa_bwd == stages 0, 1, 2.
  * Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for an unknown stage.
  */
