@@ -299,7 +299,13 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged (waits, descriptor arithmetic);
+    // tcgen05.mma and tcgen05.commit are issued by the one elected lane.
+    {
+      const uint32_t leader = elect_one();
+      auto wait = [&](int b, uint32_t parity) {
+        return mbar_wait_warp(BAR(b), parity, a.status, a.wait_limit_ns);
+      };
       constexpr uint32_t id_s = idesc_bf16_f32(128, C::BQ, false, false);  // S^T, dP^T
       constexpr uint32_t id_dv = idesc_bf16_f32(128, D, false, true);      // dV (A from TMEM)
       constexpr uint32_t id_dk = idesc_bf16_f32(128, D, false, true);      // dK
@@ -322,82 +328,81 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       auto issue_s = [&](int s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_S, dKk + koff(kk), dQk + soff(s) + koff(kk), id_s, kk > 0);
+          mma_ss(tmem + C::COL_S, dKk + koff(kk), dQk + soff(s) + koff(kk), id_s, kk > 0, leader);
       };
       auto issue_dp = [&](int s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::COL_DP, dVk + koff(kk), dOk + soff(s) + koff(kk), id_s, kk > 0);
+          mma_ss(tmem + C::COL_DP, dVk + koff(kk), dOk + soff(s) + koff(kk), id_s, kk > 0, leader);
       };
       // dV += P^T dO_i (P^T from TMEM), dK += dS^T Q_i (K-dimension = queries)
       auto issue_dv = [&](int s, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
           mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, dOmn + soff(s) + roff(kk), id_dv,
-                 (acc || kk > 0) ? 1u : 0u);
+                 (acc || kk > 0) ? 1u : 0u, leader);
       };
       auto issue_dk = [&](int s, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
           mma_ss(tmem + C::COL_DK, dSk + koff(kk), dQmn + soff(s) + roff(kk), id_dk,
-                 (acc || kk > 0) ? 1u : 0u);
+                 (acc || kk > 0) ? 1u : 0u, leader);
       };
       // dQ_i (K-dimension = keys), into the dP^T columns; both operands MN-major
       auto issue_dq = [&]() {
 #pragma unroll
         for (int kk = 0; kk < C::BK / 16; ++kk) {
-          if (C::DQ_T) mma_ss(tmem + C::COL_DP, dKmn + roff(kk), dSmn + roff(kk), id_dq, kk > 0);
-          else mma_ss(tmem + C::COL_DP, dSmn + roff(kk), dKmn + roff(kk), id_dq, kk > 0);
+          if (C::DQ_T) mma_ss(tmem + C::COL_DP, dKmn + roff(kk), dSmn + roff(kk), id_dq, kk > 0, leader);
+          else mma_ss(tmem + C::COL_DP, dSmn + roff(kk), dKmn + roff(kk), id_dq, kk > 0, leader);
         }
       };
-      bool ok = mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns) &&
-                mbar_wait(BAR(B_QFULL + 0), 0, a.status, a.wait_limit_ns) &&
-                mbar_wait(BAR(B_DOFULL + 0), 0, a.status, a.wait_limit_ns);
+      bool ok = wait(B_KV, 0) &&
+                wait(B_QFULL + 0, 0) &&
+                wait(B_DOFULL + 0, 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        mma_commit(BAR(B_SFULL));
+        mma_commit(BAR(B_SFULL), leader);
         issue_dp(0);  // dO ring slot 0
-        mma_commit(BAR(B_DPFULL));
+        mma_commit(BAR(B_DPFULL), leader);
       }
       for (int i = 0; ok && i < n_q; ++i) {
-        if (*abort_flag) { ok = false; break; }
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
         const int s = i % C::QSTAGES, so = i % C::DOSTAGES;
         const bool more = i + 1 < n_q;
         const int s1 = (i + 1) % C::QSTAGES, so1 = (i + 1) % C::DOSTAGES;
         const uint32_t ph1 = ((i + 1) / C::QSTAGES) & 1, pho1 = ((i + 1) / C::DOSTAGES) & 1;
-        if (!mbar_wait(BAR(B_PTREADY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+        if (!wait(B_PTREADY, i & 1)) { ok = false; break; }
         tc_fence_after();
         issue_dv(so, i > 0);
-        mma_commit(BAR(B_DOEMPTY + so));  // dO_i: last use was dV
+        mma_commit(BAR(B_DOEMPTY + so), leader);  // dO_i: last use was dV
         if (more) {
-          if (!mbar_wait(BAR(B_QFULL + s1), ph1, a.status, a.wait_limit_ns)) { ok = false; break; }
+          if (!wait(B_QFULL + s1, ph1)) { ok = false; break; }
           tc_fence_after();
           issue_s(s1);  // overwrites P^T(i): ordered after the dV products that read it
-          mma_commit(BAR(B_SFULL));
+          mma_commit(BAR(B_SFULL), leader);
         }
-        if (!mbar_wait(BAR(B_DSREADY), i & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+        if (!wait(B_DSREADY, i & 1)) { ok = false; break; }
         tc_fence_after();
         issue_dq();  // the dP^T columns: dP^T(i) was consumed before ds_ready
-        mma_commit(BAR(B_DQFULL));
+        mma_commit(BAR(B_DQFULL), leader);
         issue_dk(s, i > 0);
-        mma_commit(BAR(B_QEMPTY + s));  // Q_i: last use was dK
-        mma_commit(BAR(B_DSEMPTY));     // dS^T(i): last use was dQ/dK
+        mma_commit(BAR(B_QEMPTY + s), leader);  // Q_i: last use was dK
+        mma_commit(BAR(B_DSEMPTY), leader);     // dS^T(i): last use was dQ/dK
         if (more) {
           // dP^T(i+1) reuses the dQ columns once the dQ warps have read dQ(i)
-          if (!mbar_wait(BAR(B_DQEMPTY), i & 1, a.status, a.wait_limit_ns) ||
-              !mbar_wait(BAR(B_DOFULL + so1), pho1, a.status, a.wait_limit_ns)) { ok = false; break; }
+          if (!wait(B_DQEMPTY, i & 1) ||
+              !wait(B_DOFULL + so1, pho1)) { ok = false; break; }
           tc_fence_after();
           issue_dp(so1);
-          mma_commit(BAR(B_DPFULL));
+          mma_commit(BAR(B_DPFULL), leader);
         }
       }
-      if (ok) mma_commit(BAR(B_ACC));
-      else *abort_flag = 1;
-      mma_commit(BAR(B_DRAIN));
-      mbar_wait(BAR(B_DRAIN), 0, a.status, a.wait_limit_ns);
+      if (ok) mma_commit(BAR(B_ACC), leader);
+      else if (lane == 0) *abort_flag = 1;
+      mma_commit(BAR(B_DRAIN), leader);
+      wait(B_DRAIN, 0);
     }
-    __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax: P^T, dS^T
     const int wq = warp & 3;

@@ -10,7 +10,8 @@
 // Warp roles (12 warps):
 //   warp 0      TMA producer: Q tiles once, then K_j / V_j through a ring of
 //               STAGES shared-memory slots (full/empty mbarrier pairs).
-//   warp 1      TMEM allocation; lane 0 issues every tcgen05.mma:
+//   warp 1      TMEM allocation; the converged warp runs the MMA schedule
+//               and one elected lane issues every tcgen05.mma:
 //                 S_t = Q_t K_j^T   (SS form, fp32 accumulator in TMEM)
 //                 O_t += P_t V_j    (TS form: P read from TMEM, V from smem)
 //               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the
@@ -159,7 +160,10 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop converged (waits, descriptor arithmetic);
+    // tcgen05.mma and tcgen05.commit are issued by the one elected lane.
+    {
+      const uint32_t leader = elect_one();
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
       // Descriptors are built once; advancing along K only adds a byte offset
@@ -175,7 +179,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-          mma_ss(dcol, qa + off, kb + off, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(dcol, qa + off, kb + off, idesc_s, kk > 0 ? 1u : 0u, leader);
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
@@ -184,51 +188,49 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           mma_ts(dcol, acol + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_o,
-                 (acc || kk > 0) ? 1u : 0u);
+                 (acc || kk > 0) ? 1u : 0u, leader);
       };
-      bool ok = mbar_wait(BAR(B_QFULL), 0, a.status, a.wait_limit_ns);
-      ok = ok && mbar_wait(BAR(B_KFULL + 0), 0, a.status, a.wait_limit_ns);
+      auto wait = [&](int b, uint32_t parity) {
+        return mbar_wait_warp(BAR(b), parity, a.status, a.wait_limit_ns);
+      };
+      bool ok = wait(B_QFULL, 0) && wait(B_KFULL + 0, 0);
       if (ok) {
         tc_fence_after();
         for (int t = 0; t < C::QT; ++t) {
           issue_s(t, 0);
-          mma_commit(BAR(B_SFULL + t));
+          mma_commit(BAR(B_SFULL + t), leader);
         }
-        mma_commit(BAR(B_KEMPTY + 0));
+        mma_commit(BAR(B_KEMPTY + 0), leader);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        if (*abort_flag) { ok = false; break; }
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
         const bool more = j + 1 < n_kv;
         const int s1 = (j + 1) % C::STAGES;
         const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
-        if (!mbar_wait(BAR(B_VFULL + s), ph, a.status, a.wait_limit_ns)) { ok = false; break; }
+        if (!wait(B_VFULL + s, ph)) { ok = false; break; }
         for (int t = 0; t < C::QT; ++t) {
-          if (!mbar_wait(BAR(B_PFULL + t), j & 1, a.status, a.wait_limit_ns)) { ok = false; break; }
+          if (!wait(B_PFULL + t, j & 1)) { ok = false; break; }
           tc_fence_after();
           issue_pv(t, s, j > 0);
-          mma_commit(BAR(B_ODONE + t));
+          mma_commit(BAR(B_ODONE + t), leader);
           if (more) {
-            if (t == 0 && !mbar_wait(BAR(B_KFULL + s1), ph1, a.status, a.wait_limit_ns)) {
-              ok = false;
-              break;
-            }
+            if (t == 0 && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
             tc_fence_after();
             issue_s(t, s1);
-            mma_commit(BAR(B_SFULL + t));
+            mma_commit(BAR(B_SFULL + t), leader);
           }
         }
         if (!ok) break;
-        mma_commit(BAR(B_VEMPTY + s));
-        if (more) mma_commit(BAR(B_KEMPTY + s1));
+        mma_commit(BAR(B_VEMPTY + s), leader);
+        if (more) mma_commit(BAR(B_KEMPTY + s1), leader);
       }
-      if (!ok) *abort_flag = 1;
-      // drain every MMA this thread issued before TMEM can be released
-      mma_commit(BAR(B_DRAIN));
-      mbar_wait(BAR(B_DRAIN), 0, a.status, a.wait_limit_ns);
+      if (!ok && lane == 0) *abort_flag = 1;
+      // drain every MMA issued before TMEM can be released
+      mma_commit(BAR(B_DRAIN), leader);
+      wait(B_DRAIN, 0);
     }
-    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;       // query tile of this warpgroup

@@ -225,29 +225,50 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
+// One lane of a converged warp, chosen by the hardware: returns 1 there, 0
+// elsewhere. The MMA-issuing warp runs its loop with all lanes converged and
+// enables the tcgen05 issue on this lane only, so that descriptor arithmetic
+// stays warp-uniform.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(p));
+  return p;
+}
+
+// D[tmem] (+)= A[smem] * B[smem], issued only where `issue` != 0
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+                                       uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]
+// D[tmem] (+)= A[tmem] * B[smem], issued only where `issue` != 0
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
+                                       uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread has
+// completed; only where `issue` != 0.
+__device__ __forceinline__ void mma_commit(uint32_t bar, uint32_t issue) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(issue)
       : "memory");
+}
+
+// Bounded wait made warp-uniform: true only if every lane saw the phase.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int* status,
+                                               uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, limit_ns));
 }
 
 // ----------------------------------------------------------------------------
