@@ -46,7 +46,7 @@ BWD_SOURCE = os.path.join(ROOT, "exact_attention_30_gb300", "csrc", "attn_bwd_bf
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="fa", choices=["fa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
