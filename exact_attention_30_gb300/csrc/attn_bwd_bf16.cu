@@ -20,7 +20,8 @@
 //                  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T   (recompute; keys on lanes)
 //                  dV += P^T dO_i (P^T read from TMEM), dK += dS^T Q_i
 //                  dQ_i^T = K_j^T dS^T (d = 128) or dQ_i = dS K_j (d = 64)
-//                  -> fp32 atomics
+//                  -> added into the fp32 accumulator (TMA tensor reduce-add
+//                  from shared memory at d = 128, fp32 atomics at d = 64)
 //                A softmax warpgroup (one thread per key) first writes bf16
 //                P^T over the S^T columns, then, once dP^T is there, writes
 //                bf16 dS^T into a swizzled shared-memory tile that feeds both
@@ -128,7 +129,7 @@ struct BwdCfg {
   // and last by dV(i), the first product of tile i. So Q needs a deep ring
   // for its loads to run ahead, while one dO slot already gives its load
   // most of a tile of lead time.
-  static constexpr int QSTAGES = (D == 128) ? 3 : 4;
+  static constexpr int QSTAGES = (D == 128) ? 2 : 4;  // d = 128: room for the dQ staging
   static constexpr int DOSTAGES = (D == 128) ? 1 : 2;
   static constexpr int ROW_CHUNK = 128 * 128;        // 128 rows x 128 bytes, swizzled
   static constexpr int TILE = CH * ROW_CHUNK;        // 128 rows x D bf16
@@ -141,7 +142,13 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + QSTAGES * TILE;
   static constexpr int OFF_STAT = OFF_DO + DOSTAGES * TILE;
   static constexpr int STATSTAGES = 2;  // LSE*log2e and D, read by both softmax phases
-  static constexpr int OFF_BAR = OFF_STAT + STATSTAGES * STAT_BYTES;
+  // dQ reduction staging (d = 128): per dQ warp 2 x [32 queries][32 d] fp32,
+  // added into the global accumulator by the TMA engine (tensor bulk
+  // reduce-add) instead of fp32 atomics
+  static constexpr int DQ_ROWS = 32;
+  static constexpr int DQ_BLOCK_BYTES = DQ_ROWS * 32 * 4;  // 4 KB
+  static constexpr int OFF_DQS = OFF_STAT + STATSTAGES * STAT_BYTES;
+  static constexpr int OFF_BAR = OFF_DQS + (DQ_T ? 4 * 2 * DQ_BLOCK_BYTES : 0);
   // barriers: kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], st_full[2],
   //           st_empty[2], s_full, dp_full, pt_ready, ds_ready, ds_empty, dq_full,
   //           dq_empty, acc_done, drain
@@ -543,11 +550,26 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       if (lane == 0) mbar_arrive(BAR(B_DQEMPTY));
       const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;  // padded rows are scratch
       if (C::DQ_T) {
-        // lane t holds dQ[row0 + q][t] for every query q: each warp instruction
-        // adds one contiguous 128-byte segment of a dQ row
-        float* base = a.dQacc + row0 * D + t;
+        // lane t holds dQ[row0 + q][t] for every query q. Each warp stages its
+        // 32 d-columns of 32 query rows at a time ([row][32 d] fp32, 4 KB) and
+        // lets the TMA engine add the block into the accumulator; two buffers
+        // per warp, tracked by the warp's lane 0. No cross-warp barrier.
+        uint8_t* wstage = smem + C::OFF_DQS + wq * 2 * C::DQ_BLOCK_BYTES;
 #pragma unroll
-        for (int q = 0; q < NCOL; ++q) atomicAdd(base + (size_t)q * D, __uint_as_float(v[q]));
+        for (int c = 0; c < NCOL / C::DQ_ROWS; ++c) {
+          const int buf = (i * (NCOL / C::DQ_ROWS) + c) & 1;
+          if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
+          __syncwarp();
+          float* stage = reinterpret_cast<float*>(wstage + buf * C::DQ_BLOCK_BYTES);
+#pragma unroll
+          for (int q = 0; q < C::DQ_ROWS; ++q) stage[q * 32 + lane] = __uint_as_float(v[C::DQ_ROWS * c + q]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), wq * 32, (int)(row0 + (size_t)C::DQ_ROWS * c));
+            bulk_commit_group();
+          }
+        }
       } else {
         // lane t holds the whole dQ row of query row0 + t
         float4* base = reinterpret_cast<float4*>(a.dQacc + (row0 + t) * D);
@@ -557,6 +579,8 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
       }
     }
+    // every bulk reduction must be complete before the block exits
+    if (lane == 0) bulk_wait_group_all();
   }
 
   tc_fence_before();

@@ -58,6 +58,18 @@ bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int
   return r == CUDA_SUCCESS;
 }
 
+// fp32 [rows, d] accumulator as 2-D (d, rows); 32 x 32 boxes, no swizzle.
+bool encode_acc_f32(CUtensorMap* m, void* ptr, long long rows, int d) {
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_shape(int B, int H, int N, int d, float scale, fa_dtype dt) {
@@ -236,6 +248,7 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.dK = dK;
   a.dV = dV;
   a.dQacc = reinterpret_cast<float*>(ws + L.dqacc);
+  if (!encode_acc_f32(&a.tmDQacc, a.dQacc, (long long)BH * L.Npad, d)) return FA_ERR_CUDA;
   a.lse2 = reinterpret_cast<float*>(ws + L.lse2);
   a.Drow = reinterpret_cast<float*>(ws + L.drow);
   a.N = N;

@@ -42,6 +42,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st);
 
 struct BwdArgs {
   CUtensorMap tmQ, tmK, tmV, tmdO;
+  CUtensorMap tmDQacc;  // fp32 [BH*Npad, d], 32 x 32 boxes, no swizzle (d = 128 only)
   const void* O;     // bf16 [BH, N, d]
   const void* dO;    // bf16 [BH, N, d]
   const float* LSE;  // [BH, N]
