@@ -69,6 +69,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a per-rank float over the process group (identity when not distributed).
+
+    Rank 0 reports step times this way: the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_rank_step: float, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s: every rank processes its own batch (weak scaling)."""
+    return world * flops_per_rank_step / (ms_per_step_max * 1e-3) / 1e12
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -342,11 +360,7 @@ def run_gpu(args):
     pre_ms = [e[1].elapsed_time(e[2]) for e in events]
     main_ms = [e[2].elapsed_time(e[3]) for e in events]
     conv_ms = [e[3].elapsed_time(e[4]) for e in events]
-    ms_per_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), dev)
 
     # end to end through the public API with pinned host buffers
     pin = lambda t: t.pin_memory()
@@ -374,11 +388,7 @@ def run_gpu(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     nbytes = q_h.numel() * q_h.element_size()
 
     if rank != 0:
@@ -392,7 +402,7 @@ def run_gpu(args):
     achieved = BWD_FLOPS / (main_avg * 1e-3) / 1e12
     traffic = read_traffic()
     fwd_avg = mean(fwd_ms)
-    value = world * STEP_FLOPS / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(world, STEP_FLOPS, ms_per_step)
     line = {
         "metric": METRIC,
         "value": value,
@@ -426,7 +436,7 @@ def run_gpu(args):
             "step_ms_median": statistics.median(step_ms),
             "wall_ms_per_step_incl_flush": 1e3 * wall / args.steps,
         },
-        "e2e": {"value": world * STEP_FLOPS / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(world, STEP_FLOPS, e2e_ms), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": 4 * nbytes,
                 "d2h_bytes_per_step": 3 * nbytes},
         "gpu_launches": 4 * args.steps,
