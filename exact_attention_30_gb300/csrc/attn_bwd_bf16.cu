@@ -31,7 +31,8 @@
 //                MMA order is dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1), so the
 //                next tile's recompute overlaps this tile's softmax.
 //  3. dq_convert: fp32 accumulator times scale -> bf16 dQ.
-// TMEM (512 columns): S^T|P^T, dP^T|dQ, dV, dK.
+// TMEM (512 columns): S^T|P^T, dP^T|dQ, dV, dK (P^T: queries 0-63 in columns
+// 0-31, queries 64-127 in columns 64-95, bf16 pairs).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -157,8 +158,8 @@ struct BwdCfg {
   static constexpr int SMEM_MAX = 227 * 1024;
   // request 1 KB of alignment slack when it fits; the kernel checks alignment
   static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 <= SMEM_MAX) ? SMEM_BYTES + 1024 : SMEM_MAX;
-  static constexpr int THREADS = 384;
-  // TMEM columns: S^T (P^T as bf16 in its first 64), dP^T (dQ after dP^T is
+  static constexpr int THREADS = 512;  // 16 warps: producers/MMA, 2 softmax WGs, dQ WG
+  // TMEM columns: S^T (P^T as bf16 in columns 0-31 and 64-95), dP^T (dQ after dP^T is
   // consumed), dV, dK.
   static constexpr uint32_t COL_S = 0;
   static constexpr uint32_t COL_DP = 128;
@@ -171,7 +172,7 @@ struct BwdCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -213,12 +214,12 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
     }
     for (int s = 0; s < C::STATSTAGES; ++s) {
       mbar_init(BAR(B_STFULL + s), 1);
-      mbar_init(BAR(B_STEMPTY + s), 4);  // one arrival per softmax warp
+      mbar_init(BAR(B_STEMPTY + s), 8);  // one arrival per softmax warp
     }
     mbar_init(BAR(B_SFULL), 1);
     mbar_init(BAR(B_DPFULL), 1);
-    mbar_init(BAR(B_PTREADY), 4);  // one arrival per softmax warp
-    mbar_init(BAR(B_DSREADY), 4);
+    mbar_init(BAR(B_PTREADY), 8);  // one arrival per softmax warp (two warpgroups)
+    mbar_init(BAR(B_DSREADY), 8);
     mbar_init(BAR(B_DSEMPTY), 1);
     mbar_init(BAR(B_DQFULL), 1);
     mbar_init(BAR(B_DQEMPTY), 4);  // one arrival per dQ warp
@@ -346,7 +347,9 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       auto issue_dv = [&](int s, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < C::BQ / 16; ++kk)
-          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + kk * 8, dOmn + soff(s) + roff(kk), id_dv,
+          // P^T of queries 16kk..16kk+15: packed bf16 in the S^T columns of the
+          // softmax warpgroup that owns them (64 queries per group)
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + 64 * (kk >> 2) + 8 * (kk & 3), dOmn + soff(s) + roff(kk), id_dv,
                  (acc || kk > 0) ? 1u : 0u, leader);
       };
       auto issue_dk = [&](int s, bool acc) {
@@ -410,15 +413,18 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
       mma_commit(BAR(B_DRAIN), leader);
       wait(B_DRAIN, 0);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax: P^T, dS^T
+    // Two warpgroups; warpgroup g handles query columns [64g, 64g + 64) of
+    // every key row (thread = key row = TMEM lane).
+    const int g = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the tile == TMEM lane
     const bool key_live = k0 + r < N;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const uint64_t c22 = f2_pack(a.scale_log2, a.scale_log2);
     const float scale = a.scale;
-    uint8_t* dsrow = smem + C::OFF_DS + r * 128;
+    uint8_t* dsrow = smem + C::OFF_DS + g * C::ROW_CHUNK + r * 128;  // this group's dS^T chunk
     bool ok = true;
     for (int i = 0; i < n_q; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
@@ -427,15 +433,15 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
                mbar_wait(BAR(B_STFULL + st), (i / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      const float* lse2 = stat_smem + st * (C::STAT_BYTES / 4);
-      const float* drow = lse2 + C::BQ;
-      // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, over the S^T
-      // columns; 32 query columns at a time, pairs in packed fp32 arithmetic
-      uint32_t pb[64];
+      const float* lse2 = stat_smem + st * (C::STAT_BYTES / 4) + 64 * g;
+      const float* drow = stat_smem + st * (C::STAT_BYTES / 4) + C::BQ + 64 * g;
+      // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, written over
+      // this group's S^T columns (64 queries -> packed columns 64g..64g+31)
+      uint32_t pb[32];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < 2; ++h) {
         uint32_t sr[32];
-        tmem_ld32(lane_addr + C::COL_S + 32 * h, sr);
+        tmem_ld32(lane_addr + C::COL_S + 64 * g + 32 * h, sr);
         tmem_ld_wait();
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
@@ -449,23 +455,25 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
           pb[16 * h + 2 * k4 + 1] = pack_bf16x2(p2, p3);
         }
       }
-      tmem_st32(lane_addr + C::COL_S, *reinterpret_cast<uint32_t(*)[32]>(&pb[0]));
-      tmem_st32(lane_addr + C::COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&pb[32]));
+      // P^T of this group's 64 queries goes to the first 32 of its own S^T
+      // columns (64g .. 64g+31), so neither group overwrites scores the
+      // other has not read yet; the dV products take their A slices there.
+      tmem_st32(lane_addr + C::COL_S + 64 * g, pb);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_PTREADY));
-      // phase 2: dS^T = P^T o (dP^T - D) * scale, bf16, into the swizzled dS^T
-      // tile ([128 keys][64 queries] chunks; 16-byte unit c of row r lands at
-      // unit c ^ (r & 7)); 32 query columns at a time
+      // phase 2: dS'^T = P^T o (dP^T - D), bf16, into this group's swizzled
+      // [128 keys][64 queries] chunk of the dS^T tile (16-byte unit c of row r
+      // lands at unit c ^ (r & 7))
       w = mbar_wait(BAR(B_DPFULL), i & 1, a.status, a.wait_limit_ns) &&
           mbar_wait(BAR(B_DSEMPTY), (i & 1) ^ 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < 2; ++h) {
         uint32_t dr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 32 * h, dr);
+        tmem_ld32(lane_addr + C::COL_DP + 64 * g + 32 * h, dr);
         tmem_ld_wait();
         uint32_t dk[16];
 #pragma unroll
@@ -482,11 +490,10 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
           dk[2 * k4] = pack_bf16x2(ga.x, ga.y);
           dk[2 * k4 + 1] = pack_bf16x2(gb.x, gb.y);
         }
-        uint8_t* chunk_row = dsrow + (h >> 1) * C::ROW_CHUNK;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int c = (h & 1) * 4 + u;
-          *reinterpret_cast<uint4*>(chunk_row + ((c ^ (r & 7)) * 16)) =
+          const int c = h * 4 + u;
+          *reinterpret_cast<uint4*>(dsrow + ((c ^ (r & 7)) * 16)) =
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         }
       }
@@ -505,78 +512,86 @@ __global__ void __launch_bounds__(384, 1) bwd_main_kernel(const __grid_constant_
     if (!ok) {
       *abort_flag = 1;
     } else {
+      // epilogue: group 0 writes dV, group 1 writes dK (which carries the
+      // softmax scale of dS)
       tc_fence_after();
       const size_t out_row = ((size_t)bh * N + (size_t)(k0 + r)) * D;
+      const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
+      const float f = g == 0 ? 1.f : scale;
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK) + out_row;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? C::COL_DV : C::COL_DK;
-        const float f = which == 0 ? 1.f : scale;  // dK carries the softmax scale of dS
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? a.dV : a.dK) + out_row;
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t v[32];
+        tmem_ld32(lane_addr + col + 32 * q, v);
+        tmem_ld_wait();
+        if (key_live) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + col + 32 * q, v);
-          tmem_ld_wait();
-          if (key_live) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              d4[u] = make_uint4(pack_bf16x2(f * __uint_as_float(v[8 * u]), f * __uint_as_float(v[8 * u + 1])),
-                                 pack_bf16x2(f * __uint_as_float(v[8 * u + 2]), f * __uint_as_float(v[8 * u + 3])),
-                                 pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
-                                 pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
-          }
+          for (int u = 0; u < 4; ++u)
+            d4[u] = make_uint4(pack_bf16x2(f * __uint_as_float(v[8 * u]), f * __uint_as_float(v[8 * u + 1])),
+                               pack_bf16x2(f * __uint_as_float(v[8 * u + 2]), f * __uint_as_float(v[8 * u + 3])),
+                               pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
+                               pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ reduction
     const int wq = warp & 3;
     const int t = wq * 32 + lane;  // TMEM lane: d index (dQ^T) or query row (dQ)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     constexpr int NCOL = C::DQ_T ? C::BQ : D;  // columns of the dQ tile
+    constexpr int HALF = NCOL / 2;             // read in two halves (register budget)
+    uint8_t* wstage = smem + C::OFF_DQS + wq * 2 * C::DQ_BLOCK_BYTES;
+    int nblk = 0;  // staging blocks issued so far by this warp
     for (int i = 0; i < n_q; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const bool w = mbar_wait(BAR(B_DQFULL), i & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { *abort_flag = 1; break; }
       tc_fence_after();
-      uint32_t v[NCOL];
-#pragma unroll
-      for (int q = 0; q < NCOL / 32; ++q)
-        tmem_ld32(lane_addr + C::COL_DP + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * q]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_DQEMPTY));
       const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;  // padded rows are scratch
-      if (C::DQ_T) {
-        // lane t holds dQ[row0 + q][t] for every query q. Each warp stages its
-        // 32 d-columns of 32 query rows at a time ([row][32 d] fp32, 4 KB) and
-        // lets the TMA engine add the block into the accumulator; two buffers
-        // per warp, tracked by the warp's lane 0. No cross-warp barrier.
-        uint8_t* wstage = smem + C::OFF_DQS + wq * 2 * C::DQ_BLOCK_BYTES;
 #pragma unroll
-        for (int c = 0; c < NCOL / C::DQ_ROWS; ++c) {
-          const int buf = (i * (NCOL / C::DQ_ROWS) + c) & 1;
-          if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
-          __syncwarp();
-          float* stage = reinterpret_cast<float*>(wstage + buf * C::DQ_BLOCK_BYTES);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t v[HALF];
 #pragma unroll
-          for (int q = 0; q < C::DQ_ROWS; ++q) stage[q * 32 + lane] = __uint_as_float(v[C::DQ_ROWS * c + q]);
-          fence_proxy_async_smem();
+        for (int q = 0; q < HALF / 32; ++q)
+          tmem_ld32(lane_addr + C::COL_DP + HALF * hh + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * q]));
+        tmem_ld_wait();
+        if (hh == 1) {
+          // all of dQ(i) is in registers: the MMA warp may reuse the columns
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), wq * 32, (int)(row0 + (size_t)C::DQ_ROWS * c));
-            bulk_commit_group();
-          }
+          if (lane == 0) mbar_arrive(BAR(B_DQEMPTY));
         }
-      } else {
-        // lane t holds the whole dQ row of query row0 + t
-        float4* base = reinterpret_cast<float4*>(a.dQacc + (row0 + t) * D);
+        if (C::DQ_T) {
+          // lane t holds dQ[row0 + q][t] for this half's queries. Each warp
+          // stages its 32 d-columns of 32 query rows at a time ([row][32 d]
+          // fp32, 4 KB) and lets the TMA engine add the block into the
+          // accumulator; two buffers per warp, tracked by the warp's lane 0.
 #pragma unroll
-        for (int q = 0; q < D / 4; ++q)
-          atomicAdd(base + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+          for (int c = 0; c < HALF / C::DQ_ROWS; ++c, ++nblk) {
+            const int buf = nblk & 1;
+            if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
+            __syncwarp();
+            float* stage = reinterpret_cast<float*>(wstage + buf * C::DQ_BLOCK_BYTES);
+#pragma unroll
+            for (int q = 0; q < C::DQ_ROWS; ++q) stage[q * 32 + lane] = __uint_as_float(v[C::DQ_ROWS * c + q]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), wq * 32,
+                                (int)(row0 + (size_t)HALF * hh + (size_t)C::DQ_ROWS * c));
+              bulk_commit_group();
+            }
+          }
+        } else {
+          // lane t holds this half of the dQ row of query row0 + t
+          float4* base = reinterpret_cast<float4*>(a.dQacc + (row0 + t) * D + HALF * hh);
+#pragma unroll
+          for (int q = 0; q < HALF / 4; ++q)
+            atomicAdd(base + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+        }
       }
     }
     // every bulk reduction must be complete before the block exits
