@@ -53,14 +53,19 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--heads", type=int, default=None,
                    help="override H (smaller profiling captures); the JSON line names the change")
+    p.add_argument("--shape", type=int, nargs=4, metavar=("B", "H", "N", "D"), default=None,
+                   help="another [B,H,N,d] shape (the JSON line names it); the default is the "
+                        "headline shape")
     args = p.parse_args()
+    global B, H, N, D, WORKLOAD, FWD_FLOPS, BWD_FLOPS, STEP_FLOPS
+    if args.shape is not None:
+        B, H, N, D = args.shape
     if args.heads is not None:
-        global H, WORKLOAD, FWD_FLOPS, BWD_FLOPS, STEP_FLOPS
         H = args.heads
-        WORKLOAD = f"fwd+bwd bf16 B={B} H={H} N={N} d={D} non-causal"
-        FWD_FLOPS = 4.0 * B * H * N * N * D
-        BWD_FLOPS = 2.5 * FWD_FLOPS
-        STEP_FLOPS = FWD_FLOPS + BWD_FLOPS
+    WORKLOAD = f"fwd+bwd bf16 B={B} H={H} N={N} d={D} non-causal"
+    FWD_FLOPS = 4.0 * B * H * N * N * D
+    BWD_FLOPS = 2.5 * FWD_FLOPS
+    STEP_FLOPS = FWD_FLOPS + BWD_FLOPS
     return args
 
 
@@ -400,7 +405,7 @@ def run_gpu(args):
     mean = lambda xs: sum(xs) / len(xs)
     main_avg = mean(main_ms)
     achieved = BWD_FLOPS / (main_avg * 1e-3) / 1e12
-    traffic = read_traffic()
+    traffic = read_traffic() if (B, H, N, D) == (2, 16, 4096, 128) else None
     fwd_avg = mean(fwd_ms)
     value = job_throughput(world, STEP_FLOPS, ms_per_step)
     line = {
@@ -420,12 +425,12 @@ def run_gpu(args):
                    "flops_per_step": STEP_FLOPS,
                    "l2": "flushed before every step (256 MiB write, outside the per-step events)",
                    "parallelism": f"replicas x{world}, independent batches, no collective"},
-        "roofline": {"kernel": "bwd_main_kernel<128>", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": f"bwd_main_kernel<{D}>", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
                      "algorithmic_flops_per_launch": BWD_FLOPS},
         "components": {
-            "fwd": {"kernel": "fwd_bf16_kernel<128>", "ms": fwd_avg,
+            "fwd": {"kernel": f"fwd_bf16_kernel<{D}>", "ms": fwd_avg,
                     "tflops": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12,
                     "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak},
             "bwd_preprocess": {"ms": mean(pre_ms)},
