@@ -53,6 +53,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--heads", type=int, default=None,
                    help="override H (smaller profiling captures); the JSON line names the change")
+    p.add_argument("--op", default="attention", choices=["attention", "softmax"],
+                   help="softmax: time the fused row softmax on the B*H*N x N score matrix of "
+                        "the shape (HBM-bound; not the headline line)")
+    p.add_argument("--dtype", default="bf16", choices=["bf16", "f32"],
+                   help="element type for --op softmax")
     p.add_argument("--shape", type=int, nargs=4, metavar=("B", "H", "N", "D"), default=None,
                    help="another [B,H,N,d] shape (the JSON line names it); the default is the "
                         "headline shape")
@@ -455,8 +460,58 @@ def run_gpu(args):
     return 0
 
 
+def run_softmax(args):
+    """Fused row softmax over the B*H*N x N score matrix of standard attention."""
+    import torch
+
+    import exact_attention_30_gb300 as fa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    dtype = torch.bfloat16 if args.dtype == "bf16" else torch.float32
+    rows, cols = B * H * N, N
+    g = torch.Generator().manual_seed(0)
+    x = (torch.randn(rows, cols, generator=g, dtype=torch.float32) * 4).to(dtype).to(dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        fa.fa_softmax_rows(x, scale=1.0, out=y)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        fa.fa_softmax_rows(x, scale=1.0, out=y)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    nbytes = 2 * x.numel() * x.element_size()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, src = read_peaks()
+    line = {
+        "metric": "fused row softmax GB/s (HBM-bound)", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "data": "synthetic",
+        "config": {"workload": f"row softmax of the {rows} x {cols} score matrix "
+                               f"(B={B} H={H} N={N}), {args.dtype} in and out",
+                   "l2": "input and output each larger than L2"},
+        "roofline": {"kernel": "softmax_warp_kernel" if cols <= 2048 else "softmax_block_kernel",
+                     "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "softmax":
+        return run_softmax(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -21,7 +21,7 @@ import re
 import torch
 
 __all__ = [
-    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes", "fa_check_device_status",
+    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes", "fa_softmax_rows", "fa_check_device_status",
     "fa_debug_timeout_probe", "fa_status_string", "fa_version", "library_path", "load_library",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_F32", "FA_BF16", "FAError", "FA_BWD_PREPROCESS", "FA_BWD_MAIN", "FA_BWD_DQ_CONVERT",
@@ -42,6 +42,7 @@ _SIGNATURES = {
     "fa_bwd": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_stage": (_ci, [_ci] + [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_noalloc": (_ci, [_vp] * 9 + [_ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_softmax_rows": (_ci, [_vp, _vp, _ci, _ci, _cf, _ci, _vp]),
     "fa_check_device_status": (_ci, [_vp]),
     "fa_debug_timeout_probe": (_ci, [ctypes.c_longlong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_ci]),
@@ -186,6 +187,21 @@ def fa_bwd_stage(stage: int, q, k, v, o, do, lse, scale: float | None = None, wo
                  dq=None, dk=None, dv=None):
     """One backward stage (FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT) on ``workspace``."""
     return _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv)
+
+
+def fa_softmax_rows(x, scale: float = 1.0, out=None):
+    """Row softmax of a CUDA tensor (last dimension = row), fp32 or bf16; returns ``out``."""
+    lib = load_library()
+    _check(x, "x")
+    cols = x.shape[-1]
+    rows = x.numel() // max(cols, 1)
+    y = torch.empty_like(x) if out is None else out
+    _check(y, "out", x)
+    with torch.cuda.device(x.device):
+        rc = lib.fa_softmax_rows(x.data_ptr(), y.data_ptr(), rows, cols, float(scale),
+                                 _dtype_code(x), _stream_ptr(x.device))
+    _raise(rc, "fa_softmax_rows")
+    return y
 
 
 def fa_check_device_status(device=None) -> int:

@@ -29,6 +29,7 @@ SOURCES = [
     ("attn_fwd_bf16.cu", []),
     ("attn_bwd_bf16.cu", []),
     ("fa_noalloc.cu", []),
+    ("softmax_rows.cu", []),
 ]
 
 

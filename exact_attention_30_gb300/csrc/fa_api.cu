@@ -287,6 +287,21 @@ fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, c
 }
 
 
+fa_status fa_softmax_rows(const void* X, void* Y, int rows, int cols, float scale, fa_dtype dt,
+                          void* stream) {
+  if (!X || !Y || rows < 1 || cols < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dt != FA_F32 && dt != FA_BF16) return FA_ERR_INVALID_ARG;
+  const size_t es = dt == FA_BF16 ? 2 : 4;
+  if (!aligned(X, es) || !aligned(Y, es)) return FA_ERR_INVALID_ARG;
+  if (cols > kSoftmaxMaxCols) return FA_ERR_UNSUPPORTED;
+  if ((long long)rows * cols >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  return launch_softmax_rows(X, Y, rows, cols, scale, dt == FA_BF16,
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 fa_status fa_check_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;

@@ -65,6 +65,11 @@ constexpr int kBwdRowPad = 128;
 // height); must match BwdCfg<d>::BQ.
 constexpr int bwd_query_tile(int d) { return d > 0 ? 128 : 128; }
 
+// Fused row softmax (softmax_rows.cu): rows x cols, fp32 or bf16, cols <= 32768.
+constexpr int kSoftmaxMaxCols = 32768;
+cudaError_t launch_softmax_rows(const void* X, void* Y, int rows, int cols, float scale, bool bf16,
+                                cudaStream_t st);
+
 // Bounded-wait probe (fa_debug_timeout_probe).
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
 

@@ -112,6 +112,19 @@ fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, c
                        float scale, fa_dtype dt, void* stream);
 
 /*
+ * Fused row softmax: Y[r, :] = softmax(scale * X[r, :]) for each of `rows`
+ * rows of `cols` elements. The fusion example of "FlashAttention and Triton"
+ * §19.11: one pass per row (a ragged tail reads as -inf), max, exp, sum and
+ * divide without intermediate arrays, so each element is read and written
+ * once. X, Y: dense row-major [rows, cols], dtype `dt` (fp32 or bf16, the
+ * arithmetic in fp32); they may alias (in place). 1 <= cols <= 32768,
+ * rows >= 1, rows * cols < 2^31, scale finite and > 0.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (cols > 32768), FA_ERR_CUDA.
+ */
+fa_status fa_softmax_rows(const void* X, void* Y, int rows, int cols, float scale, fa_dtype dt,
+                          void* stream);
+
+/*
  * fa_bwd without a caller-provided workspace, for callers that cannot
  * allocate device memory (for example code running inside a host application
  * that owns all device memory through its own pool, or a serving path where

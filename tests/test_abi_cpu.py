@@ -82,3 +82,11 @@ def test_python_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         fa.fa_fwd(q, q, q)
+
+
+def test_softmax_rows_rejects_bad_arguments_before_launch(lib):
+    assert lib.fa_softmax_rows(0, FAKE, 4, 16, 1.0, fa.FA_F32, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_softmax_rows(FAKE, FAKE, 0, 16, 1.0, fa.FA_F32, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_softmax_rows(FAKE, FAKE, 4, 16, 0.0, fa.FA_F32, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_softmax_rows(FAKE + 1, FAKE, 4, 16, 1.0, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_softmax_rows(FAKE, FAKE, 4, 32769, 1.0, fa.FA_F32, None) == fa.FA_ERR_UNSUPPORTED
