@@ -53,9 +53,12 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--heads", type=int, default=None,
                    help="override H (smaller profiling captures); the JSON line names the change")
-    p.add_argument("--op", default="attention", choices=["attention", "softmax"],
+    p.add_argument("--op", default="attention", choices=["attention", "softmax", "decode"],
                    help="softmax: time the fused row softmax on the B*H*N x N score matrix of "
-                        "the shape (HBM-bound; not the headline line)")
+                        "the shape; decode: time KV-cache decode on --decode-workload (both "
+                        "HBM-bound; not the headline line)")
+    p.add_argument("--decode-workload", default="decode_bf16_8x32x1x32768x128",
+                   help="named decode workload for --op decode")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "f32"],
                    help="element type for --op softmax")
     p.add_argument("--shape", type=int, nargs=4, metavar=("B", "H", "N", "D"), default=None,
@@ -508,10 +511,65 @@ def run_softmax(args):
     return 0
 
 
+def run_decode(args):
+    """KV-cache decode (fa_decode: split kernel + combine kernel) on a named workload."""
+    import torch
+
+    import exact_attention_30_gb300 as fa
+    from exact_attention_30_gb300.inputs import DECODE_WORKLOADS, decode_inputs
+
+    w = DECODE_WORKLOADS[args.decode_workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    q, k, v = (t.to(dev) for t in decode_inputs(w, seed=0))
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d), dtype=torch.uint8,
+                     device=dev)
+    splits, kps = fa.fa_decode_plan(w.B, w.H, w.Nq, w.Nk, w.d)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: fa.fa_decode(q, k, v, w.scale, out=o, lse=lse, workspace=ws)
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    nbytes = w.hbm_bytes()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, src = read_peaks()
+    line = {
+        "metric": "KV-cache decode GB/s (HBM-bound)", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H={w.H} Nq={w.Nq} Nk={w.Nk} d={w.d}, "
+                               f"{splits} key ranges of {kps}",
+                   "l2": "K and V larger than L2 (no flush)",
+                   "tflops": w.flops() / (ms * 1e-3) / 1e12},
+        "roofline": {"kernel": "decode_split_kernel + decode_combine_kernel (one fa_decode call)",
+                     "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{src} copy bandwidth",
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.op == "softmax":
         return run_softmax(args)
+    if args.op == "decode":
+        return run_decode(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -10,6 +10,7 @@ CUDA kernels; there is no CPU path. If the shared library has not been built
 
     o, lse = fa_fwd(q, k, v, scale)                 # q,k,v: [B,H,N,d] cuda
     dq, dk, dv = fa_bwd(q, k, v, o, do, lse, scale)
+    o, lse = fa_decode(q_new, k_cache, v_cache, scale)   # q_new: [B,H,Nq<=8,d]
 """
 from __future__ import annotations
 
@@ -21,7 +22,8 @@ import re
 import torch
 
 __all__ = [
-    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes", "fa_softmax_rows", "fa_check_device_status",
+    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes", "fa_softmax_rows", "fa_decode",
+    "fa_decode_workspace_bytes", "fa_decode_plan", "fa_check_device_status",
     "fa_debug_timeout_probe", "fa_status_string", "fa_version", "library_path", "load_library",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
     "FA_F32", "FA_BF16", "FAError", "FA_BWD_PREPROCESS", "FA_BWD_MAIN", "FA_BWD_DQ_CONVERT",
@@ -43,6 +45,9 @@ _SIGNATURES = {
     "fa_bwd_stage": (_ci, [_ci] + [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_noalloc": (_ci, [_vp] * 9 + [_ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_softmax_rows": (_ci, [_vp, _vp, _ci, _ci, _cf, _ci, _vp]),
+    "fa_decode": (_ci, [_vp] * 6 + [_sz, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_decode_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
+    "fa_decode_plan": (_ci, [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci), ctypes.POINTER(_ci)]),
     "fa_check_device_status": (_ci, [_vp]),
     "fa_debug_timeout_probe": (_ci, [ctypes.c_longlong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_ci]),
@@ -202,6 +207,52 @@ def fa_softmax_rows(x, scale: float = 1.0, out=None):
                                  _dtype_code(x), _stream_ptr(x.device))
     _raise(rc, "fa_softmax_rows")
     return y
+
+
+def fa_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, dtype=torch.bfloat16) -> int:
+    """Scratch bytes fa_decode needs on the current device."""
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F32
+    return int(load_library().fa_decode_workspace_bytes(B, H, Nq, Nk, d, code))
+
+
+def fa_decode_plan(B: int, H: int, Nq: int, Nk: int, d: int, resident_ctas: int = 0):
+    """(splits, keys_per_split) that fa_decode uses; resident_ctas > 0 plans without a device."""
+    s, k = ctypes.c_int(0), ctypes.c_int(0)
+    _raise(load_library().fa_decode_plan(B, H, Nq, Nk, d, int(resident_ctas), ctypes.byref(s),
+                                         ctypes.byref(k)), "fa_decode_plan")
+    return s.value, k.value
+
+
+def fa_decode(q, k, v, scale: float | None = None, out=None, lse=None, workspace=None):
+    """KV-cache decode: q [B,H,Nq,d] (Nq <= 8) against k, v [B,H,Nk,d], bf16.
+
+    Returns (O like q, LSE [B,H,Nq] float32).
+    """
+    lib = load_library()
+    _check(q, "q")
+    _check(k, "k")
+    _check(v, "v", k)
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B,H,Nq,d] and k, v [B,H,Nk,d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d or k.dtype != q.dtype or k.device != q.device:
+        raise ValueError("k, v must be [B,H,Nk,d] with q's B, H, d, dtype and device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "out", q)
+    if lse.dtype != torch.float32 or lse.shape != (B, H, Nq) or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [B,H,Nq] on the same device")
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            ws_bytes = fa_decode_workspace_bytes(B, H, Nq, Nk, d, q.dtype)
+            workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+        rc = lib.fa_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                           B, H, Nq, Nk, d, scale, _dtype_code(q), _stream_ptr(q.device))
+    _raise(rc, "fa_decode")
+    return o, lse
 
 
 def fa_check_device_status(device=None) -> int:

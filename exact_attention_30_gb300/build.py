@@ -30,6 +30,7 @@ SOURCES = [
     ("attn_bwd_bf16.cu", []),
     ("fa_noalloc.cu", []),
     ("softmax_rows.cu", []),
+    ("decode_splitkv.cu", []),
 ]
 
 

@@ -302,6 +302,93 @@ fa_status fa_softmax_rows(const void* X, void* Y, int rows, int cols, float scal
              : FA_ERR_CUDA;
 }
 
+}  // extern "C"
+
+namespace {
+fa_status check_decode(int B, int H, int Nq, int Nk, int d, fa_dtype dt) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (dt != FA_F32 && dt != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (dt != FA_BF16 || (d != 64 && d != 128)) return FA_ERR_UNSUPPORTED;
+  if (Nq > kDecodeMaxQueries || Nk > (1 << 30)) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+struct DecodeLayout {
+  DecodePlan plan;
+  size_t opart, lsepart, total;
+};
+DecodeLayout decode_layout(int B, int H, int Nq, int Nk, int d) {
+  DecodeLayout L{};
+  L.plan = plan_decode(B * H, Nq, Nk, d);
+  if (L.plan.splits < 1) return L;
+  const size_t rows = (size_t)B * H * Nq;
+  L.opart = 0;
+  L.lsepart = align_up((size_t)L.plan.splits * rows * d * sizeof(float), 256);
+  L.total = L.lsepart + align_up((size_t)L.plan.splits * rows * sizeof(float), 256);
+  return L;
+}
+}  // namespace
+
+extern "C" {
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, fa_dtype dt) {
+  if (check_decode(B, H, Nq, Nk, d, dt) != FA_OK) return 0;
+  return decode_layout(B, H, Nq, Nk, d).total;
+}
+
+fa_status fa_decode_plan(int B, int H, int Nq, int Nk, int d, int resident_ctas, int* splits,
+                         int* keys_per_split) {
+  if (!splits || !keys_per_split || resident_ctas < 0) return FA_ERR_INVALID_ARG;
+  const fa_status s = check_decode(B, H, Nq, Nk, d, FA_BF16);
+  if (s != FA_OK) return s;
+  const DecodePlan p = resident_ctas > 0 ? plan_decode_for_slots(B * H, Nk, resident_ctas)
+                                         : plan_decode(B * H, Nq, Nk, d);
+  if (p.splits < 1) return FA_ERR_CUDA;
+  *splits = p.splits;
+  *keys_per_split = p.keys_per_split;
+  return FA_OK;
+}
+
+fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk, int d,
+                    float scale, fa_dtype dt, void* stream) {
+  fa_status s = check_decode(B, H, Nq, Nk, d, dt);
+  if (s != FA_OK) return s;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!Q || !K || !V || !O || !LSE || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
+      !aligned(LSE, 4) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  const DecodeLayout L = decode_layout(B, H, Nq, Nk, d);
+  if (L.plan.splits < 1) return FA_ERR_CUDA;
+  if (workspace_bytes < L.total) return FA_ERR_INVALID_ARG;
+  if (!get_encode_fn()) return FA_ERR_CUDA;
+  int* status = device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  const int BH = B * H;
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bhnd_bf16(&a.tmK, K, BH, Nk, d, 64) || !encode_bhnd_bf16(&a.tmV, V, BH, Nk, d, 64))
+    return FA_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  a.Q = Q;
+  a.O = O;
+  a.LSE = LSE;
+  a.Opart = reinterpret_cast<float*>(ws + L.opart);
+  a.LSEpart = reinterpret_cast<float*>(ws + L.lsepart);
+  a.BH = BH;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.splits = L.plan.splits;
+  a.keys_per_split = L.plan.keys_per_split;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.wait_limit_ns = kDefaultWaitLimitNs;
+  return launch_decode_bf16(a, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                     : FA_ERR_CUDA;
+}
+
 fa_status fa_check_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;

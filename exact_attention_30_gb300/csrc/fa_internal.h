@@ -70,6 +70,32 @@ constexpr int kSoftmaxMaxCols = 32768;
 cudaError_t launch_softmax_rows(const void* X, void* Y, int rows, int cols, float scale, bool bf16,
                                 cudaStream_t st);
 
+// ---- KV-cache decode (decode_splitkv.cu) ----
+constexpr int kDecodeMaxQueries = 8;
+constexpr int kDecodeMaxSplits = 256;
+struct DecodeArgs {
+  CUtensorMap tmK, tmV;  // [BH, Nk, d] bf16 as 3-D (d, Nk, BH), 64 x 64 boxes, 128-byte swizzle
+  const void* Q;         // bf16 [BH, Nq, d]
+  void* O;               // bf16 [BH, Nq, d]
+  float* LSE;            // [BH, Nq], natural log
+  float* Opart;          // fp32 [splits, BH*Nq, d]: each split's normalised output
+  float* LSEpart;        // fp32 [splits, BH*Nq]: each split's log-sum-exp, base 2
+  int BH, Nq, Nk, splits, keys_per_split;
+  float scale_log2;
+  int* status;
+  unsigned long long wait_limit_ns;
+};
+struct DecodePlan {
+  int splits;          // 0 on failure
+  int keys_per_split;  // a multiple of 64
+};
+// Split count for a problem on the current device (queries its SM count and
+// the kernel's occupancy once per device).
+DecodePlan plan_decode(int BH, int Nq, int Nk, int d);
+// The same choice for a given number of resident CTAs on the GPU.
+DecodePlan plan_decode_for_slots(int BH, int Nk, int slots);
+cudaError_t launch_decode_bf16(const DecodeArgs& a, int d, cudaStream_t st);
+
 // Bounded-wait probe (fa_debug_timeout_probe).
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
 

@@ -17,6 +17,18 @@ Workloads (every one non-causal, Q/K/V/dO i.i.d. N(0, 1)):
   N=16384 d=128, every key row with n % 64 == 0 multiplied by 4 after the
   bf16 cast (exact: a power of two) so that the running max keeps moving.
 
+KV-cache decode workloads (``DECODE_WORKLOADS``; the pages describe decoding
+with a KV cache but print no decode configuration, so these stand in for a
+serving step: one new query per sequence, or a group of queries that share a
+K/V head):
+
+* ``decode_bf16_8x32x1x32768x128`` -- B=8, H=32, Nq=1, Nk=32768, d=128.
+* ``decode_bf16_8x8x8x32768x128`` -- B=8, H=8 K/V heads, Nq=8 queries per
+  K/V head, Nk=32768, d=128.
+
+Decode inputs are drawn like the others (Q [B,H,Nq,d], then K and V
+[B,H,Nk,d], every 64th key row times 4).
+
 bf16 workloads: ``torch.Generator().manual_seed(seed)``, ``torch.randn`` in
 float32 of shape [B, H, N, d] in the order Q, K, V, dO, then round-to-nearest
 to bf16.
@@ -106,3 +118,43 @@ def workload_inputs(w: Workload, seed: int = 0):
         return t(Q), t(K), t(V), None
     return random_qkv(w.B, w.H, w.N, w.d, w.torch_dtype, seed=seed, with_do=w.bwd,
                       big_key_every=w.big_key_every)
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.d)))
+
+    def flops(self) -> float:
+        """4 * B * H * Nq * Nk * d (scores and P V)."""
+        return 4.0 * self.B * self.H * self.Nq * self.Nk * self.d
+
+    def hbm_bytes(self) -> float:
+        """Bytes a decode call must move: K and V once, Q and O once (bf16), LSE (fp32)."""
+        kv = 2 * self.B * self.H * self.Nk * self.d * 2
+        qo = 2 * self.B * self.H * self.Nq * self.d * 2
+        return float(kv + qo + self.B * self.H * self.Nq * 4)
+
+
+DECODE_WORKLOADS = {
+    w.name: w
+    for w in [
+        DecodeWorkload("decode_bf16_8x32x1x32768x128", 8, 32, 1, 32768, 128),
+        DecodeWorkload("decode_bf16_8x8x8x32768x128", 8, 8, 8, 32768, 128),
+    ]
+}
+
+
+def decode_inputs(w: DecodeWorkload, seed: int = 0):
+    """(q, k, v) CPU bf16 tensors of a decode workload."""
+    q, k, v, _ = random_qkv(w.B, w.H, w.Nq, w.d, torch.bfloat16, seed=seed, with_do=False,
+                            big_key_every=64, n_k=w.Nk)
+    return q, k, v

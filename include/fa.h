@@ -125,6 +125,51 @@ fa_status fa_softmax_rows(const void* X, void* Y, int rows, int cols, float scal
                           void* stream);
 
 /*
+ * KV-cache decode: attention of Nq new queries per head against Nk cached
+ * keys and values, O = softmax(scale * Q K^T) V and LSE = ln sum exp(scale *
+ * Q K^T) per query row, every query seeing every key (no mask). The use case
+ * is the inference remark of "Interview Q15: FlashAttention" (decoding with a
+ * KV cache). The keys are cut into contiguous splits processed in parallel,
+ * each with the online softmax of "Lesson 1: FlashAttention core idea" §3;
+ * the split results (normalised output and log-sum-exp) are merged with the
+ * same (m, l) rule by a second kernel. Nothing of size Nq x Nk reaches
+ * global memory.
+ *   Q, O : [B,H,Nq,d] bf16 (for grouped-query attention pass the G query
+ *          heads that share one K/V head as Nq = G rows).
+ *   K, V : [B,H,Nk,d] bf16, the cache; only the first Nk rows are read.
+ *   LSE  : [B,H,Nq] float32 output (natural log, as fa_fwd).
+ *   workspace : device scratch of >= fa_decode_workspace_bytes() bytes,
+ *          256-byte aligned, not used by another call in flight; contents on
+ *          entry do not matter (split outputs and log-sum-exps, fp32).
+ *   dt   : FA_BF16 only; d in {64, 128}; 1 <= Nq <= 8; 1 <= Nk <= 2^30;
+ *          B*H <= 65535. Q, K, V, O 16-byte aligned, LSE 4-byte aligned.
+ * Errors: FA_ERR_INVALID_ARG (pointers, sizes, scale, small workspace),
+ * FA_ERR_UNSUPPORTED (FA_F32, d, Nq > 8), FA_ERR_CUDA.
+ */
+fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk, int d,
+                    float scale, fa_dtype dt, void* stream);
+
+/*
+ * Bytes of scratch fa_decode needs for this problem on the CURRENT device
+ * (the split count depends on its SM count); 0 on invalid arguments or a
+ * failed device query.
+ */
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d, fa_dtype dt);
+
+/*
+ * The split plan fa_decode uses: *splits key ranges of *keys_per_split keys
+ * (a multiple of 64; the last range may be shorter), chosen to fill whole
+ * waves of resident CTAs. resident_ctas > 0 plans for a GPU that holds that
+ * many decode CTAs at once (no device access, for tests and capacity
+ * planning); resident_ctas == 0 queries the current device. Returns
+ * FA_ERR_INVALID_ARG on bad sizes or null outputs, FA_ERR_CUDA if the device
+ * query fails.
+ */
+fa_status fa_decode_plan(int B, int H, int Nq, int Nk, int d, int resident_ctas, int* splits,
+                         int* keys_per_split);
+
+/*
  * fa_bwd without a caller-provided workspace, for callers that cannot
  * allocate device memory (for example code running inside a host application
  * that owns all device memory through its own pool, or a serving path where

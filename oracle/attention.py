@@ -29,6 +29,13 @@ library primitive used as a step):
 * ``online_softmax_stats`` -- the (m, l) recurrence of "Lesson 1" §3 over a
   list of score blocks, for the worked example of "FlashAttention and Triton"
   §19.5 (scores [1, 2] then [3, 4]).
+* ``merge_partials`` / ``split_kv_attention_fwd`` -- the same (m, l) rule
+  applied to whole results: attention over disjoint key ranges computed
+  separately, then merged. This is how decoding against a KV cache (the
+  inference remark of "Interview Q15") is parallelised over the keys. The
+  reference for decode parity is still ``attention_fwd`` on the rectangular
+  problem (N_q new queries, N_k cached keys); the split form is checked
+  against it.
 
 Readings where the pages are silent (each also listed in the design notes):
 * ``scale`` is a free argument; the pages fix 1/sqrt(d). dS carries exactly one
@@ -57,6 +64,8 @@ __all__ = [
     "online_softmax_stats",
     "attention_fwd_batched",
     "attention_bwd_batched",
+    "merge_partials",
+    "split_kv_attention_fwd",
 ]
 
 
@@ -223,3 +232,33 @@ def attention_bwd_batched(Q, K, V, dO, scale: float, heads=None):
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
         dQ[b, h], dK[b, h], dV[b, h] = attention_bwd(Q[b, h], K[b, h], V[b, h], dO[b, h], scale)
     return dQ, dK, dV
+
+
+def merge_partials(O_parts, LSE_parts):
+    """Merge attention results over disjoint key ranges: (O, LSE).
+
+    Each part s covers some of the keys and gives its normalised output O_s
+    [N_q, d_v] and log-sum-exp LSE_s = m_s + ln(l_s) [N_q]. The rule of
+    "Lesson 1" §3 (m = max of the maxima, each l rescaled by exp(m_s - m)),
+    with l_s exp(m_s - m) = exp(LSE_s - m):
+      m = max_s LSE_s,  w_s = exp(LSE_s - m),  l = sum_s w_s,
+      O = sum_s w_s O_s / l,  LSE = m + ln(l).
+    """
+    L = np.stack([_f64(x) for x in LSE_parts])          # [S, N_q]
+    Os = np.stack([_f64(x) for x in O_parts])           # [S, N_q, d_v]
+    m = L.max(axis=0)
+    w = np.exp(L - m[None, :])
+    l = w.sum(axis=0)
+    O = (w[:, :, None] * Os).sum(axis=0) / l[:, None]
+    return O, m + np.log(l)
+
+
+def split_kv_attention_fwd(Q, K, V, scale: float, keys_per_split: int):
+    """``attention_fwd`` over key ranges of ``keys_per_split`` keys, then ``merge_partials``.
+
+    Ranges are [0, k), [k, 2k), ...; the last one holds what remains.
+    """
+    K, V = _f64(K), _f64(V)
+    k = int(keys_per_split)
+    parts = [attention_fwd(Q, K[s:s + k], V[s:s + k], scale) for s in range(0, K.shape[0], k)]
+    return merge_partials([p[0] for p in parts], [p[1] for p in parts])

@@ -12,8 +12,9 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import (attention_bwd, attention_fwd, attention_fwd_rows, online_softmax_stats,
-                    row_softmax, scores, tiled_attention_fwd)
+from oracle import (attention_bwd, attention_fwd, attention_fwd_rows, merge_partials,
+                    online_softmax_stats, row_softmax, scores, split_kv_attention_fwd,
+                    tiled_attention_fwd)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -257,3 +258,38 @@ def test_D_identity_rowsum_dP_P_equals_rowsum_dO_O():
     O, _ = attention_fwd(Q, K, V, scale)
     dP = dO @ V.T
     assert np.abs((dP * P).sum(axis=1) - (dO * O).sum(axis=1)).max() <= 1e-12
+
+
+# ---------------------------------------------------------------- split-KV merge
+@pytest.mark.parametrize("nq,nk,kps", [(1, 1, 1), (1, 200, 64), (3, 7, 3), (8, 130, 64), (2, 50, 50)])
+def test_split_kv_merge_equals_one_shot(nq, nk, kps):
+    """Merging per-range results reproduces attention over all keys (the pages'
+    claim that the online (m, l) update is exact), to rounding."""
+    rng = np.random.default_rng(nq * 1000 + nk)
+    Q, K, V = rng.normal(size=(nq, 16)), rng.normal(size=(nk, 16)), rng.normal(size=(nk, 16))
+    O1, L1 = attention_fwd(Q, K, V, 0.25)
+    O2, L2 = split_kv_attention_fwd(Q, K, V, 0.25, kps)
+    assert np.abs(O1 - O2).max() < 1e-12
+    assert np.abs(L1 - L2).max() < 1e-12
+
+
+def test_split_merge_on_the_worked_example():
+    """The worked example's score row [1, 2, 3, 4] as two key ranges of two:
+    one query q = [1], keys k_j = [j], scale 1. The merged log-sum-exp is the
+    closed form 4 + ln(1 + e^-1 + e^-2 + e^-3), and with values v_j = [j] the
+    merged output is sum_j j e^(j-4) / l."""
+    Q = np.array([[1.0]])
+    K = np.array([[1.0], [2.0], [3.0], [4.0]])
+    V = K.copy()
+    O, L = split_kv_attention_fwd(Q, K, V, 1.0, 2)
+    l = 1 + math.exp(-1) + math.exp(-2) + math.exp(-3)
+    assert abs(L[0] - (4 + math.log(l))) < 1e-14
+    expect = sum(j * math.exp(j - 4) for j in range(1, 5)) / l
+    assert abs(O[0, 0] - expect) < 1e-14
+
+
+def test_merge_of_a_dominant_range_returns_it():
+    """A range whose log-sum-exp exceeds the others by far carries all weight."""
+    O_a, O_b = np.full((1, 2), 3.0), np.full((1, 2), -5.0)
+    O, L = merge_partials([O_a, O_b], [np.array([800.0]), np.array([0.0])])
+    assert np.allclose(O, 3.0, rtol=0, atol=1e-300) and abs(L[0] - 800.0) < 1e-12
