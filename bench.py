@@ -61,6 +61,9 @@ def parse_args():
                    help="named decode workload for --op decode")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "f32"],
                    help="element type for --op softmax")
+    p.add_argument("--causal", action="store_true",
+                   help="causal attention (FLOPs counted as half of the full count, the usual "
+                        "convention; the JSON line names it)")
     p.add_argument("--shape", type=int, nargs=4, metavar=("B", "H", "N", "D"), default=None,
                    help="another [B,H,N,d] shape (the JSON line names it); the default is the "
                         "headline shape")
@@ -70,8 +73,8 @@ def parse_args():
         B, H, N, D = args.shape
     if args.heads is not None:
         H = args.heads
-    WORKLOAD = f"fwd+bwd bf16 B={B} H={H} N={N} d={D} non-causal"
-    FWD_FLOPS = 4.0 * B * H * N * N * D
+    WORKLOAD = f"fwd+bwd bf16 B={B} H={H} N={N} d={D} " + ("causal" if args.causal else "non-causal")
+    FWD_FLOPS = 4.0 * B * H * N * N * D * (0.5 if args.causal else 1.0)
     BWD_FLOPS = 2.5 * FWD_FLOPS
     STEP_FLOPS = FWD_FLOPS + BWD_FLOPS
     return args
@@ -315,13 +318,16 @@ def run_gpu(args):
     ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
+    causal = bool(args.causal)
+
     def bwd_stage(stage):
-        fa.fa_bwd_stage(stage, q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv)
+        fa.fa_bwd_stage(stage, q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv,
+                        causal=causal)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse, causal=causal)
         if ev is not None:
             ev[1].record(stream)
         bwd_stage(fa.FA_BWD_PREPROCESS)
@@ -386,8 +392,8 @@ def run_gpu(args):
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
         do.copy_(hdo, non_blocking=True)
-        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
-        fa.fa_bwd(q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse, causal=causal)
+        fa.fa_bwd(q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv, causal=causal)
         hdq.copy_(dq, non_blocking=True)
         hdk.copy_(dk, non_blocking=True)
         hdv.copy_(dv, non_blocking=True)
@@ -413,7 +419,7 @@ def run_gpu(args):
     mean = lambda xs: sum(xs) / len(xs)
     main_avg = mean(main_ms)
     achieved = BWD_FLOPS / (main_avg * 1e-3) / 1e12
-    traffic = read_traffic() if (B, H, N, D) == (2, 16, 4096, 128) else None
+    traffic = read_traffic() if (B, H, N, D) == (2, 16, 4096, 128) and not causal else None
     fwd_avg = mean(fwd_ms)
     value = job_throughput(world, STEP_FLOPS, ms_per_step)
     line = {
@@ -455,7 +461,9 @@ def run_gpu(args):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if causal:
+        line["config"]["flop_count"] = "causal: half of 4*B*H*N^2*d forward, 2.5x that backward"
+    if world == 1 and not args.no_cpu_baseline and not causal:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -11,6 +11,8 @@ CUDA kernels; there is no CPU path. If the shared library has not been built
     o, lse = fa_fwd(q, k, v, scale)                 # q,k,v: [B,H,N,d] cuda
     dq, dk, dv = fa_bwd(q, k, v, o, do, lse, scale)
     o, lse = fa_decode(q_new, k_cache, v_cache, scale)   # q_new: [B,H,Nq<=8,d]
+    o, lse = fa_fwd(q, k, v, causal=True)            # causal self-attention
+    o, lse = fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen)   # packed [total,H,d]
 """
 from __future__ import annotations
 
@@ -22,7 +24,8 @@ import re
 import torch
 
 __all__ = [
-    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_workspace_bytes", "fa_softmax_rows", "fa_decode",
+    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_fwd_varlen", "fa_bwd_varlen",
+    "fa_bwd_varlen_workspace_bytes", "FA_CAUSAL", "fa_bwd_workspace_bytes", "fa_softmax_rows", "fa_decode",
     "fa_decode_workspace_bytes", "fa_decode_plan", "fa_check_device_status",
     "fa_debug_timeout_probe", "fa_status_string", "fa_version", "library_path", "load_library",
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT",
@@ -32,6 +35,8 @@ __all__ = [
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_F32, FA_BF16 = 0, 1
 FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT = 0, 1, 2
+FA_CAUSAL = 1
+_STAGE_FLAGS = {FA_BWD_PREPROCESS: 1 << 8, FA_BWD_MAIN: 2 << 8, FA_BWD_DQ_CONVERT: 4 << 8}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
@@ -40,6 +45,11 @@ _lib = None
 _vp, _ci, _cf, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGNATURES = {
     "fa_fwd": (_ci, [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
+    "fa_fwd_ex": (_ci, [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
+    "fa_fwd_varlen": (_ci, [_vp] * 6 + [_ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
+    "fa_bwd_ex": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
+    "fa_bwd_varlen_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
+    "fa_bwd_varlen": (_ci, [_vp] * 11 + [_sz, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
     "fa_bwd": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_stage": (_ci, [_ci] + [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
@@ -126,7 +136,7 @@ def _raise(code: int, where: str):
         raise FAError(code, where)
 
 
-def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None):
+def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False):
     """Forward pass: returns (O [B,H,N,d] like q, LSE [B,H,N] float32)."""
     lib = load_library()
     _check(q, "q")
@@ -142,8 +152,9 @@ def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None):
     if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_cuda:
         raise ValueError("lse must be float32 [B,H,N] on the same device")
     with torch.cuda.device(q.device):
-        rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                        B, H, N, d, scale, _dtype_code(q), _stream_ptr(q.device))
+        rc = lib.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           B, H, N, d, scale, FA_CAUSAL if causal else 0, _dtype_code(q),
+                           _stream_ptr(q.device))
     _raise(rc, "fa_fwd")
     return o, lse
 
@@ -153,7 +164,7 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int, dtype=torch.bfloat16)
     return int(load_library().fa_bwd_workspace_bytes(B, H, N, d, code))
 
 
-def _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv):
+def _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv, causal=False):
     lib = load_library()
     _check(q, "q")
     for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
@@ -170,28 +181,96 @@ def _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv):
     dv = torch.empty_like(q) if dv is None else dv
     for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
         _check(t, n, q)
-    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
-            workspace.numel() * workspace.element_size(), B, H, N, d, scale, _dtype_code(q),
-            _stream_ptr(q.device))
+    if stage is not None and stage not in _STAGE_FLAGS:
+        raise ValueError(f"unknown backward stage {stage}")
+    flags = (FA_CAUSAL if causal else 0) | (0 if stage is None else _STAGE_FLAGS[stage])
     with torch.cuda.device(q.device):
-        if stage is None:
-            _raise(lib.fa_bwd(*args), "fa_bwd")
-        else:
-            _raise(lib.fa_bwd_stage(int(stage), *args), "fa_bwd_stage")
+        rc = lib.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                           lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                           B, H, N, d, scale, flags, _dtype_code(q), _stream_ptr(q.device))
+    _raise(rc, "fa_bwd" if stage is None else "fa_bwd_stage")
     return dq, dk, dv
 
 
 def fa_bwd(q, k, v, o, do, lse, scale: float | None = None, workspace=None, dq=None, dk=None,
-           dv=None):
+           dv=None, causal: bool = False):
     """Backward pass: returns (dQ, dK, dV), each like q."""
-    return _bwd_call(None, q, k, v, o, do, lse, scale, workspace, dq, dk, dv)
+    return _bwd_call(None, q, k, v, o, do, lse, scale, workspace, dq, dk, dv, causal)
 
 
 def fa_bwd_stage(stage: int, q, k, v, o, do, lse, scale: float | None = None, workspace=None,
-                 dq=None, dk=None, dv=None):
+                 dq=None, dk=None, dv=None, causal: bool = False):
     """One backward stage (FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT) on ``workspace``."""
-    return _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv)
+    return _bwd_call(stage, q, k, v, o, do, lse, scale, workspace, dq, dk, dv, causal)
+
+
+def _check_varlen(q, cu_seqlens, max_seqlen):
+    _check(q, "q")
+    if q.dim() != 3:
+        raise ValueError("packed tensors are [total, H, d]")
+    if not isinstance(cu_seqlens, torch.Tensor) or not cu_seqlens.is_cuda or \
+            cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous int32 CUDA tensor [B+1]")
+    if cu_seqlens.device != q.device:
+        raise ValueError("cu_seqlens must be on q's device")
+    total, H, d = q.shape
+    return cu_seqlens.numel() - 1, H, total, int(max_seqlen), d
+
+
+def fa_bwd_varlen_workspace_bytes(B: int, H: int, total: int, max_seqlen: int, d: int,
+                                  dtype=torch.bfloat16) -> int:
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F32
+    return int(load_library().fa_bwd_varlen_workspace_bytes(B, H, total, max_seqlen, d, code))
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, scale: float | None = None,
+                  causal: bool = False, out=None, lse=None):
+    """Packed variable-length forward: q, k, v [total, H, d]; cu_seqlens int32 [B+1] on the GPU.
+
+    Returns (O [total, H, d] like q, LSE [H, total] float32).
+    """
+    lib = load_library()
+    B, H, total, max_seqlen, d = _check_varlen(q, cu_seqlens, max_seqlen)
+    _check(k, "k", q)
+    _check(v, "v", q)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check(o, "out", q)
+    if lse.dtype != torch.float32 or lse.shape != (H, total) or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [H, total] on the same device")
+    with torch.cuda.device(q.device):
+        rc = lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               cu_seqlens.data_ptr(), B, H, total, max_seqlen, d, scale,
+                               FA_CAUSAL if causal else 0, _dtype_code(q), _stream_ptr(q.device))
+    _raise(rc, "fa_fwd_varlen")
+    return o, lse
+
+
+def fa_bwd_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen: int, scale: float | None = None,
+                  causal: bool = False, workspace=None):
+    """Backward of ``fa_fwd_varlen``: returns (dQ, dK, dV), each [total, H, d] like q."""
+    lib = load_library()
+    B, H, total, max_seqlen, d = _check_varlen(q, cu_seqlens, max_seqlen)
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check(t, n, q)
+    if lse.dtype != torch.float32 or lse.shape != (H, total) or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous float32 [H, total] on the same device")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            n = fa_bwd_varlen_workspace_bytes(B, H, total, max_seqlen, d, q.dtype)
+            workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+        rc = lib.fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                               cu_seqlens.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), B, H, total, max_seqlen,
+                               d, scale, FA_CAUSAL if causal else 0, _dtype_code(q),
+                               _stream_ptr(q.device))
+    _raise(rc, "fa_bwd_varlen")
+    return dq, dk, dv
 
 
 def fa_softmax_rows(x, scale: float = 1.0, out=None):

@@ -33,12 +33,21 @@
 //  3. dq_convert: fp32 accumulator times scale -> bf16 dQ.
 // TMEM (512 columns): S^T|P^T, dP^T|dQ, dV, dK (P^T: queries 0-63 in columns
 // 0-31, queries 64-127 in columns 64-95, bf16 pairs).
+//
+// Sequences (SeqArgs): preprocess and convert work on rows of whole planes;
+// the main kernel works on one sequence of the layout. Keys past the
+// sequence's end give P = 0 on their rows, queries past it (the next
+// sequence of a packed batch) P = 0 in their columns. Causal attention
+// visits only the query tiles at or after the key tile's diagonal and masks
+// the diagonal tile (key r, query q: P = 0 where r > q); the grid then lists
+// the key tiles with the most query tiles first.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -47,24 +56,27 @@ namespace {
 // 1. preprocess
 // ----------------------------------------------------------------------------
 // One group of D/8 lanes per row; each lane reads 8 bf16 of O and dO.
+// Rows of whole planes: plane p, row n < ws_rows; rows n < total are data
+// (of whichever sequence holds them), the rest padding.
 template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, int BH) {
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   constexpr int LPR = D / 8;            // lanes per row
   constexpr int RPW = 32 / LPR;         // rows per warp
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane / LPR, l = lane % LPR;
-  const long long prow = (long long)warp_global * RPW + sub;  // padded row index
-  const long long total = (long long)BH * a.Npad;
+  const long long prow = (long long)warp_global * RPW + sub;  // workspace row index
+  const long long total = (long long)a.planes * a.ws_rows;
   float acc = 0.f;
   bool live = false;
-  long long bh = 0, n = 0;
+  long long plane = 0, n = 0;
   if (prow < total) {
-    bh = prow / a.Npad;
-    n = prow - bh * a.Npad;
-    live = n < a.N;
+    plane = prow / a.ws_rows;
+    n = prow - plane * a.ws_rows;
+    live = n < a.seq.total;
     if (live) {
-      const size_t off = ((size_t)bh * a.N + (size_t)n) * D + (size_t)l * 8;
+      const size_t off = (size_t)plane * (size_t)a.seq.plane_stride + (size_t)n * (size_t)a.seq.row_stride +
+                         (size_t)l * 8;
       const uint4 uo = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.O) + off);
       const uint4 ud = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.dO) + off);
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&uo);
@@ -87,7 +99,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, int BH) {
   // one fused multiply-add and dP - D with one add (exact when they are equal).
   if (prow < total && l == 0) {
     a.Drow[prow] = live ? -acc : 0.f;
-    a.lse2[prow] = live ? -a.LSE[(size_t)bh * a.N + (size_t)n] * 1.4426950408889634f : -INFINITY;
+    a.lse2[prow] = live ? -a.LSE[(size_t)plane * (size_t)a.seq.stat_plane + (size_t)n] * 1.4426950408889634f
+                        : -INFINITY;
   }
 }
 
@@ -95,14 +108,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a, int BH) {
 // 3. dQ convert
 // ----------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, int BH) {
+__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 elements
-  const long long groups = (long long)BH * a.N * (D / 8);
+  const long long groups = (long long)a.planes * a.seq.total * (D / 8);
   if (idx >= groups) return;
   const long long row = idx / (D / 8);
   const int g = (int)(idx - row * (D / 8));
-  const long long bh = row / a.N, n = row - bh * a.N;
-  const float4* src = reinterpret_cast<const float4*>(a.dQacc + ((size_t)bh * a.Npad + n) * D + g * 8);
+  const long long plane = row / a.seq.total, n = row - plane * a.seq.total;
+  const float4* src = reinterpret_cast<const float4*>(a.dQacc + ((size_t)plane * a.ws_rows + n) * D + g * 8);
   const float4 x = src[0], y = src[1];
   uint4 u;
   const float f = a.scale;  // the softmax scale of dS, applied once here
@@ -110,7 +123,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, int BH
   u.y = pack_bf16x2(f * x.z, f * x.w);
   u.z = pack_bf16x2(f * y.x, f * y.y);
   u.w = pack_bf16x2(f * y.z, f * y.w);
-  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dQ) + (size_t)row * D + g * 8) = u;
+  *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dQ) + (size_t)plane * (size_t)a.seq.plane_stride +
+                             (size_t)n * (size_t)a.seq.row_stride + g * 8) = u;
 }
 
 // ----------------------------------------------------------------------------
@@ -197,10 +211,20 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   const float* stat_smem = reinterpret_cast<const float*>(smem + C::OFF_STAT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int k0 = blockIdx.x * C::BK;
-  const int N = a.N;
-  const int n_q = a.Npad / C::BQ;
+  const bool causal = a.seq.causal != 0;
+  // causal grids list bh fastest and the key tiles in increasing order (the
+  // first key tiles see the most query tiles)
+  const int bh = causal ? (int)blockIdx.x : (int)blockIdx.y;
+  const int kb = causal ? (int)blockIdx.y : (int)blockIdx.x;
+  const SeqView sv = seq_view(a.seq, bh, a.status);
+  const int N = sv.len;  // queries = keys of this sequence
+  const int k0 = kb * C::BK;
+  if (k0 >= N) return;  // the whole CTA: no key of this sequence here
+  const int n_q = (N + C::BQ - 1) / C::BQ;
+  const int i_begin = causal ? kb : 0;  // query tiles before the diagonal see no key of this tile
+  const int n_it = n_q - i_begin;       // >= 1
+  const int y0 = sv.start, plane = sv.plane;
+  const size_t ws_row0 = (size_t)plane * a.ws_rows + (size_t)y0;  // workspace row of query 0
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_KV), 1);
@@ -213,7 +237,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       mbar_init(BAR(B_DOEMPTY + s), 1);
     }
     for (int s = 0; s < C::STATSTAGES; ++s) {
-      mbar_init(BAR(B_STFULL + s), 1);
+      mbar_init(BAR(B_STFULL + s), 1);   // the statistics warp's lane 0
       mbar_init(BAR(B_STEMPTY + s), 8);  // one arrival per softmax warp
     }
     mbar_init(BAR(B_SFULL), 1);
@@ -242,13 +266,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tma_prefetch_desc(&a.tmV);
       mbar_arrive_expect_tx(BAR(B_KV), 2 * C::TILE);
       for (int c = 0; c < C::CH; ++c) {
-        tma_load_3d(sbase + C::OFF_K + c * C::ROW_CHUNK, &a.tmK, BAR(B_KV), c * 64, k0, bh);
-        tma_load_3d(sbase + C::OFF_V + c * C::ROW_CHUNK, &a.tmV, BAR(B_KV), c * 64, k0, bh);
+        tma_load_3d(sbase + C::OFF_K + c * C::ROW_CHUNK, &a.tmK, BAR(B_KV), c * 64, y0 + k0, plane);
+        tma_load_3d(sbase + C::OFF_V + c * C::ROW_CHUNK, &a.tmV, BAR(B_KV), c * 64, y0 + k0, plane);
       }
       int last[C::QSTAGES];
 #pragma unroll
       for (int s = 0; s < C::QSTAGES; ++s) last[s] = -1;
-      for (int i = 0; i < n_q; ++i) {
+      for (int i = 0; i < n_it; ++i) {  // i: iteration; query tile i_begin + i
         if (*abort_flag) break;
         const int s = i % C::QSTAGES;
         const uint32_t ph = (i / C::QSTAGES) & 1;
@@ -256,7 +280,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         mbar_arrive_expect_tx(BAR(B_QFULL + s), C::TILE);
         for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
-                      c * 64, i * C::BQ, bh);
+                      c * 64, y0 + (i_begin + i) * C::BQ, plane);
         last[s] = i;
       }
       mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns);
@@ -267,42 +291,48 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ producer: stats, dO ring
-    if (lane == 0) {
-      tma_prefetch_desc(&a.tmdO);
-      int last[C::DOSTAGES], last_st[C::STATSTAGES];
-#pragma unroll
-      for (int s = 0; s < C::DOSTAGES; ++s) last[s] = -1;
-#pragma unroll
-      for (int s = 0; s < C::STATSTAGES; ++s) last_st[s] = -1;
-      for (int i = 0; i < n_q; ++i) {
-        if (*abort_flag) break;
-        {
-          const int t = i % C::STATSTAGES;
-          const uint32_t pt = (i / C::STATSTAGES) & 1;
-          if (!mbar_wait(BAR(B_STEMPTY + t), pt ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-          mbar_arrive_expect_tx(BAR(B_STFULL + t), C::STAT_BYTES);
-          const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;
-          bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES, a.lse2 + row0, C::BQ * 4, BAR(B_STFULL + t));
-          bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES + C::BQ * 4, a.Drow + row0, C::BQ * 4,
-                    BAR(B_STFULL + t));
-          last_st[t] = i;
+    // The whole warp copies each query tile's two statistics rows (lane k
+    // takes rows 4k..4k+3; a sequence may start at any row, so these are
+    // plain loads) and lane 0 issues the dO tile loads.
+    if (lane == 0) tma_prefetch_desc(&a.tmdO);
+    int last = -1;  // lane 0: last dO tile issued
+    for (int i = 0; i < n_it; ++i) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      {
+        const int t = i % C::STATSTAGES;
+        const uint32_t pt = (i / C::STATSTAGES) & 1;
+        if (!mbar_wait_warp(BAR(B_STEMPTY + t), pt ^ 1, a.status, a.wait_limit_ns)) {
+          if (lane == 0) *abort_flag = 1;
+          break;
         }
+        const size_t row0 = ws_row0 + (size_t)(i_begin + i) * C::BQ + 4 * lane;
+        float* dst = reinterpret_cast<float*>(smem + C::OFF_STAT + t * C::STAT_BYTES) + 4 * lane;
+        const float4 l4 = make_float4(a.lse2[row0], a.lse2[row0 + 1], a.lse2[row0 + 2], a.lse2[row0 + 3]);
+        const float4 d4 = make_float4(a.Drow[row0], a.Drow[row0 + 1], a.Drow[row0 + 2], a.Drow[row0 + 3]);
+        *reinterpret_cast<float4*>(dst) = l4;
+        *reinterpret_cast<float4*>(dst + C::BQ) = d4;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_STFULL + t));
+      }
+      if (lane == 0) {
         const int s = i % C::DOSTAGES;
         const uint32_t ph = (i / C::DOSTAGES) & 1;
-        if (!mbar_wait(BAR(B_DOEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(BAR(B_DOFULL + s), C::TILE);
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
-                      BAR(B_DOFULL + s), c * 64, i * C::BQ, bh);
-        last[s] = i;
+        if (!mbar_wait(BAR(B_DOEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) {
+          *abort_flag = 1;
+        } else {
+          mbar_arrive_expect_tx(BAR(B_DOFULL + s), C::TILE);
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
+                        BAR(B_DOFULL + s), c * 64, y0 + (i_begin + i) * C::BQ, plane);
+          last = i;
+        }
       }
-#pragma unroll
-      for (int s = 0; s < C::DOSTAGES; ++s)
-        if (last[s] >= 0) mbar_wait(BAR(B_DOFULL + s), (last[s] / C::DOSTAGES) & 1, a.status, a.wait_limit_ns);
-#pragma unroll
-      for (int s = 0; s < C::STATSTAGES; ++s)
-        if (last_st[s] >= 0)
-          mbar_wait(BAR(B_STFULL + s), (last_st[s] / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
+      __syncwarp();
+    }
+    if (lane == 0) {
+      // the last dO load issued into each slot must have landed before exit
+      for (int i = last - C::DOSTAGES + 1 < 0 ? 0 : last - C::DOSTAGES + 1; i <= last; ++i)
+        mbar_wait(BAR(B_DOFULL + i % C::DOSTAGES), (i / C::DOSTAGES) & 1, a.status, a.wait_limit_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -376,10 +406,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         issue_dp(0);  // dO ring slot 0
         mma_commit(BAR(B_DPFULL), leader);
       }
-      for (int i = 0; ok && i < n_q; ++i) {
+      for (int i = 0; ok && i < n_it; ++i) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
         const int s = i % C::QSTAGES, so = i % C::DOSTAGES;
-        const bool more = i + 1 < n_q;
+        const bool more = i + 1 < n_it;
         const int s1 = (i + 1) % C::QSTAGES, so1 = (i + 1) % C::DOSTAGES;
         const uint32_t ph1 = ((i + 1) / C::QSTAGES) & 1, pho1 = ((i + 1) / C::DOSTAGES) & 1;
         if (!wait(B_PTREADY, i & 1)) { ok = false; break; }
@@ -421,14 +451,21 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the tile == TMEM lane
     const bool key_live = k0 + r < N;
+    const int qc0 = 64 * g;  // first query column of this group
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const uint64_t c22 = f2_pack(a.scale_log2, a.scale_log2);
     const float scale = a.scale;
     uint8_t* dsrow = smem + C::OFF_DS + g * C::ROW_CHUNK + r * 128;  // this group's dS^T chunk
     bool ok = true;
-    for (int i = 0; i < n_q; ++i) {
+    for (int i = 0; i < n_it; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       const int st = i % C::STATSTAGES;
+      const int qi = i_begin + i;  // query tile
+      // columns q of this tile with P = 0: q >= q_end (past the sequence) and,
+      // on the causal diagonal, q < r (key r after query q)
+      const int q_end = N - qi * C::BQ;
+      const int q_min = (causal && qi == kb) ? r : 0;
+      const bool mask_cols = q_end < C::BQ || (causal && qi == kb);
       bool w = mbar_wait(BAR(B_SFULL), i & 1, a.status, a.wait_limit_ns) &&
                mbar_wait(BAR(B_STFULL + st), (i / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -451,6 +488,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           const float2 xb = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4 + 2]), __uint_as_float(sr[4 * k4 + 3])), c22, f2_pack(nl.z, nl.w)));
           float p0 = ex2_approx(xa.x), p1 = ex2_approx(xa.y), p2 = ex2_approx(xb.x), p3 = ex2_approx(xb.y);
           if (!key_live) p0 = p1 = p2 = p3 = 0.f;
+          if (mask_cols) {
+            const int q = qc0 + 32 * h + 4 * k4;
+            p0 = (q < q_min || q >= q_end) ? 0.f : p0;
+            p1 = (q + 1 < q_min || q + 1 >= q_end) ? 0.f : p1;
+            p2 = (q + 2 < q_min || q + 2 >= q_end) ? 0.f : p2;
+            p3 = (q + 3 < q_min || q + 3 >= q_end) ? 0.f : p3;
+          }
           pb[16 * h + 2 * k4] = pack_bf16x2(p0, p1);
           pb[16 * h + 2 * k4 + 1] = pack_bf16x2(p2, p3);
         }
@@ -515,7 +559,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       // epilogue: group 0 writes dV, group 1 writes dK (which carries the
       // softmax scale of dS)
       tc_fence_after();
-      const size_t out_row = ((size_t)bh * N + (size_t)(k0 + r)) * D;
+      const size_t out_row = key_live ? seq_row_offset(a.seq, sv, k0 + r) : 0;
       const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
       const float f = g == 0 ? 1.f : scale;
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK) + out_row;
@@ -544,12 +588,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     constexpr int HALF = NCOL / 2;             // read in two halves (register budget)
     uint8_t* wstage = smem + C::OFF_DQS + wq * 2 * C::DQ_BLOCK_BYTES;
     int nblk = 0;  // staging blocks issued so far by this warp
-    for (int i = 0; i < n_q; ++i) {
+    for (int i = 0; i < n_it; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const bool w = mbar_wait(BAR(B_DQFULL), i & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { *abort_flag = 1; break; }
       tc_fence_after();
-      const size_t row0 = (size_t)bh * a.Npad + (size_t)i * C::BQ;  // padded rows are scratch
+      // rows past the sequence receive exact zeros (their P is 0)
+      const size_t row0 = ws_row0 + (size_t)(i_begin + i) * C::BQ;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[HALF];
@@ -612,10 +657,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
   cudaError_t e = cudaSuccess;
   if (stages & kStagePre) {
     constexpr int RPW = 32 / (D / 8);
-    const long long rows = (long long)BH * a.Npad;
+    const long long rows = (long long)a.planes * a.ws_rows;
     const long long warps = (rows + RPW - 1) / RPW;
     const long long blocks = (warps * 32 + 255) / 256;
-    bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a, BH);
+    bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -623,14 +668,15 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
     e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + C::BK - 1) / C::BK, BH);
+    const unsigned kblocks = (unsigned)((a.seq.N + C::BK - 1) / C::BK);
+    const dim3 grid = a.seq.causal ? dim3((unsigned)BH, kblocks) : dim3(kblocks, (unsigned)BH);
     bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (stages & kStageConvert) {
-    const long long groups = (long long)BH * a.N * (D / 8);
-    dq_convert_kernel<D><<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(a, BH);
+    const long long groups = (long long)a.planes * a.seq.total * (D / 8);
+    dq_convert_kernel<D><<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(a);
     e = cudaGetLastError();
   }
   return e;

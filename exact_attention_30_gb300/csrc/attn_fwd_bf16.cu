@@ -30,6 +30,14 @@
 // columns it came from (the A operand of the TS MMA).
 // Epilogue: O / l to bf16, LSE = (m_ref + log2 l) * ln 2, rows >= N skipped.
 //
+// Sequences: a CTA works on one sequence of the SeqArgs layout (fixed length,
+// or one entry of a packed variable-length batch); keys past the sequence's
+// end are masked like a ragged tail. Causal attention (query row r sees keys
+// c <= r) visits only the key tiles up to each query tile's diagonal and
+// masks the diagonal tile; the grid then lists the CTAs with the most key
+// tiles first (longest-processing-time order), so the short ones fill the
+// last wave.
+//
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word, drains its in-flight TMA loads and MMAs, frees TMEM and
 // exits.
@@ -39,6 +47,7 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace fa {
 namespace {
@@ -88,10 +97,23 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * (C::BM * C::QT);
-  const int N = a.N;
+  const bool causal = a.seq.causal != 0;
+  // causal grids list bh fastest and the query blocks from the last (most key
+  // tiles) to the first
+  const int bh = causal ? (int)blockIdx.x : (int)blockIdx.y;
+  const int qblk = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.x;
+  const SeqView sv = seq_view(a.seq, bh, a.status);
+  const int N = sv.len;  // queries = keys of this sequence
+  const int q0 = qblk * (C::BM * C::QT);
+  if (q0 >= N) return;  // the whole CTA: nothing of this sequence here
   const int n_kv = (N + C::BN - 1) / C::BN;
+  // key tiles per query tile: all of them, or up to the diagonal
+  const int qt0 = q0 / C::BM;
+  const int n_t0 = causal ? min(qt0 + 1, n_kv) : n_kv;
+  const int n_t1 = causal ? min(qt0 + 2, n_kv) : n_kv;  // >= n_t0
+  const int n_max = n_t1;
+  const int y0 = sv.start;  // first row of the sequence in the TMA views
+  const int plane = sv.plane;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_QFULL), 1);
@@ -126,11 +148,11 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       for (int t = 0; t < C::QT; ++t)
         for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_Q + (t * C::CH + c) * C::CHUNK_BYTES, &a.tmQ, BAR(B_QFULL),
-                      c * 64, q0 + t * C::BM, bh);
+                      c * 64, y0 + q0 + t * C::BM, plane);
       int last_k[C::STAGES], last_v[C::STAGES];  // last tile loaded into each slot
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) last_k[s] = last_v[s] = -1;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < n_max; ++j) {
         if (*abort_flag) break;
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
@@ -138,13 +160,13 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         mbar_arrive_expect_tx(BAR(B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmK,
-                      BAR(B_KFULL + s), c * 64, j * C::BN, bh);
+                      BAR(B_KFULL + s), c * 64, y0 + j * C::BN, plane);
         last_k[s] = j;
         if (!mbar_wait(BAR(B_VEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(BAR(B_VFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmV,
-                      BAR(B_VFULL + s), c * 64, j * C::BN, bh);
+                      BAR(B_VFULL + s), c * 64, y0 + j * C::BN, plane);
         last_v[s] = j;
       }
       // drain: the last load issued into each slot must have landed before exit
@@ -202,21 +224,24 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         }
         mma_commit(BAR(B_KEMPTY + 0), leader);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
+      for (int j = 0; ok && j < n_max; ++j) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
-        const bool more = j + 1 < n_kv;
         const int s1 = (j + 1) % C::STAGES;
         const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
         if (!wait(B_VFULL + s, ph)) { ok = false; break; }
+        bool k_next = false;  // K_{j+1} has landed
         for (int t = 0; t < C::QT; ++t) {
+          const int n_own = t == 0 ? n_t0 : n_t1;
+          if (j >= n_own) continue;  // this query tile is past its diagonal
           if (!wait(B_PFULL + t, j & 1)) { ok = false; break; }
           tc_fence_after();
           issue_pv(t, s, j > 0);
           mma_commit(BAR(B_ODONE + t), leader);
-          if (more) {
-            if (t == 0 && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
+          if (j + 1 < n_own) {
+            if (!k_next && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
+            k_next = true;
             tc_fence_after();
             issue_s(t, s1);
             mma_commit(BAR(B_SFULL + t), leader);
@@ -224,7 +249,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         }
         if (!ok) break;
         mma_commit(BAR(B_VEMPTY + s), leader);
-        if (more) mma_commit(BAR(B_KEMPTY + s1), leader);
+        if (j + 1 < n_max) mma_commit(BAR(B_KEMPTY + s1), leader);
       }
       if (!ok && lane == 0) *abort_flag = 1;
       // drain every MMA issued before TMEM can be released
@@ -236,30 +261,34 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
     const int t = (warp - 4) >> 2;       // query tile of this warpgroup
     const int wq = warp & 3;             // TMEM lane quarter
     const int row_in_tile = wq * 32 + lane;
-    const int row = q0 + t * C::BM + row_in_tile;
+    const int row = q0 + t * C::BM + row_in_tile;  // within the sequence
+    const int n_own = t == 0 ? n_t0 : n_t1;
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + C::S_COL(t);
     const uint32_t o_addr = lane_addr + C::O_COL(t);
     const float c2 = a.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    for (int j = 0; j < n_own; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       bool w = mbar_wait(BAR(B_SFULL + t), j & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       // Raw scores of this row, 64 columns at a time (two 32-column loads, one
-      // wait); columns past N read as -inf.
+      // wait). Only the last key tile of a query tile can hold masked columns:
+      // keys past the sequence's end, and (causal) keys after this row.
       uint32_t r[64];
-      const int valid = N - j * C::BN;
+      const bool mask_tile = j == n_own - 1;
+      int valid = N - j * C::BN;
+      if (causal) valid = min(valid, row - j * C::BN + 1);
       auto load_half = [&](int h) {
         tmem_ld32(s_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
         tmem_ld32(s_addr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         tmem_ld_wait();
-        if (valid < C::BN) {
+        if (mask_tile) {
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            if (64 * h + i >= valid) r[i] = __float_as_uint(-INFINITY);
+            r[i] = 64 * h + i >= valid ? __float_as_uint(-INFINITY) : r[i];
         }
       };
       // Speculative pass: exponentiate against the current reference max while
@@ -345,8 +374,8 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       if (lane == 0) mbar_arrive(BAR(B_PFULL + t));
     }
     tmem_st_wait();  // no TMEM store may be in flight when the loop is left early
-    if (ok && n_kv > 0) {
-      const bool w = mbar_wait(BAR(B_ODONE + t), (n_kv - 1) & 1, a.status, a.wait_limit_ns);
+    if (ok && n_own > 0) {
+      const bool w = mbar_wait(BAR(B_ODONE + t), (n_own - 1) & 1, a.status, a.wait_limit_ns);
       ok = __all_sync(0xffffffffu, w);
     }
     if (!ok) {
@@ -354,8 +383,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
     } else {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow =
-          reinterpret_cast<__nv_bfloat16*>(a.O) + ((size_t)bh * N + (size_t)row) * D;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) + seq_row_offset(a.seq, sv, row);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t r[32];
@@ -374,7 +402,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
           }
         }
       }
-      if (row < N) a.LSE[(size_t)bh * N + row] = (m_ref + __log2f(l)) * 0.69314718055994531f;
+      if (row < N) a.LSE[seq_stat_index(a.seq, sv, row)] = (m_ref + __log2f(l)) * 0.69314718055994531f;
     }
   }
 
@@ -393,7 +421,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, int BH, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + C::BM * C::QT - 1) / (C::BM * C::QT), BH);
+  const unsigned qblocks = (unsigned)((a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT));
+  const dim3 grid = a.seq.causal ? dim3((unsigned)BH, qblocks) : dim3(qblocks, (unsigned)BH);
   fwd_bf16_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
   return cudaGetLastError();
 }

@@ -44,11 +44,12 @@ bool get_encode_fn() {
   return true;
 }
 
-// [BH, N, d] bf16 viewed as 3-D (d, N, BH); box 64 x box_rows x 1, 128-byte
-// swizzle. Rows past N within a head read as zero.
-bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows) {
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+// A bf16 tensor of the SeqArgs layout viewed as 3-D (d, rows, planes); box
+// 64 x box_rows x 1, 128-byte swizzle. Rows past `total` read as zero.
+bool encode_seq_bf16(CUtensorMap* m, const void* ptr, const SeqArgs& sq, int planes, int d,
+                     int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)sq.total, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)sq.row_stride * 2, (cuuint64_t)sq.plane_stride * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
@@ -56,6 +57,15 @@ bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// [BH, N, d] bf16 (the fixed-length layout).
+bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int box_rows) {
+  SeqArgs sq{};
+  sq.total = N;
+  sq.row_stride = d;
+  sq.plane_stride = (long long)N * d;
+  return encode_seq_bf16(m, ptr, sq, BH, d, box_rows);
 }
 
 // fp32 [rows, d] accumulator as 2-D (d, rows); 32 x 32 boxes, no swizzle.
@@ -72,39 +82,90 @@ bool encode_acc_f32(CUtensorMap* m, void* ptr, long long rows, int d) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+fa_status check_dtype_d(int d, fa_dtype dt) {
+  if (dt != FA_F32 && dt != FA_BF16) return FA_ERR_INVALID_ARG;
+  if (dt == FA_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dt == FA_F32 && d > 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 fa_status check_shape(int B, int H, int N, int d, float scale, fa_dtype dt) {
   if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (dt != FA_F32 && dt != FA_BF16) return FA_ERR_INVALID_ARG;
   const long long BH = (long long)B * H;
-  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // grid.y
+  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // a grid dimension
   if (BH * (long long)N * d >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
-  if (dt == FA_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (dt == FA_F32 && d > 128) return FA_ERR_UNSUPPORTED;
-  return FA_OK;
+  return check_dtype_d(d, dt);
+}
+
+fa_status check_varlen(const int* cu_seqlens, int B, int H, int total, int max_seqlen, int d,
+                       float scale, fa_dtype dt) {
+  if (!cu_seqlens || !aligned(cu_seqlens, 4)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || total < 1 || max_seqlen < 1 || max_seqlen > total || d < 1)
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (dt != FA_F32 && dt != FA_BF16) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
+  if ((long long)total * H * d >= (1ll << 31)) return FA_ERR_UNSUPPORTED;
+  return check_dtype_d(d, dt);
+}
+
+SeqArgs fixed_seq(int H, int N, int d, bool causal) {
+  SeqArgs sq{};
+  sq.cu_seqlens = nullptr;
+  sq.H = H;
+  sq.N = N;
+  sq.total = N;
+  sq.causal = causal ? 1 : 0;
+  sq.row_stride = d;
+  sq.plane_stride = (long long)N * d;
+  sq.stat_plane = N;
+  return sq;
+}
+
+SeqArgs varlen_seq(const int* cu_seqlens, int H, int total, int max_seqlen, int d, bool causal) {
+  SeqArgs sq{};
+  sq.cu_seqlens = cu_seqlens;
+  sq.H = H;
+  sq.N = max_seqlen;
+  sq.total = total;
+  sq.causal = causal ? 1 : 0;
+  sq.row_stride = (long long)H * d;
+  sq.plane_stride = d;
+  sq.stat_plane = total;
+  return sq;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdWorkspaceLayout {
   size_t dqacc, lse2, drow, total;
-  int Npad;
+  int planes, ws_rows;
 };
-BwdWorkspaceLayout bwd_layout(int B, int H, int N, int d, fa_dtype dt) {
+// fp32: D per row ([planes, total]). bf16: fp32 dQ accumulator
+// [planes, ws_rows, d] and two per-row statistics [planes, ws_rows].
+BwdWorkspaceLayout bwd_layout(const SeqArgs& sq, int B, int d, fa_dtype dt) {
   BwdWorkspaceLayout L{};
-  const size_t BH = (size_t)B * H;
+  L.planes = sq.cu_seqlens ? sq.H : B * sq.H;
+  const size_t P = (size_t)L.planes;
   if (dt == FA_F32) {
-    L.Npad = N;
+    L.ws_rows = sq.total;
     L.drow = 0;
-    L.total = align_up(BH * N * sizeof(float), 256);
+    L.total = align_up(P * sq.total * sizeof(float), 256);
     return L;
   }
-  L.Npad = (N + kBwdRowPad - 1) / kBwdRowPad * kBwdRowPad;
+  L.ws_rows = (sq.total + kBwdRowPad - 1) / kBwdRowPad * kBwdRowPad + (sq.cu_seqlens ? kBwdRowPad : 0);
   L.dqacc = 0;
-  L.lse2 = align_up(BH * L.Npad * d * sizeof(float), 256);
-  L.drow = L.lse2 + align_up(BH * L.Npad * sizeof(float), 256);
-  L.total = L.drow + align_up(BH * L.Npad * sizeof(float), 256);
+  L.lse2 = align_up(P * L.ws_rows * d * sizeof(float), 256);
+  L.drow = L.lse2 + align_up(P * L.ws_rows * sizeof(float), 256);
+  L.total = L.drow + align_up(P * L.ws_rows * sizeof(float), 256);
   return L;
+}
+
+unsigned flag_stages(int flags) {
+  const unsigned m = ((unsigned)flags >> 8) & 7u;
+  return m == 0 ? kStageAll : m;
 }
 
 }  // namespace
@@ -147,6 +208,101 @@ cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaS
 
 using namespace fa;
 
+namespace {
+
+fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                   const SeqArgs& sq, int B, int d, float scale, fa_dtype dt, void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  const size_t al = dt == FA_BF16 ? 16 : 4;
+  if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) || !aligned(LSE, 4))
+    return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * sq.H;
+  const int planes = sq.cu_seqlens ? sq.H : BH;
+  int* status = device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  if (dt == FA_F32) {
+    return launch_fwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
+                          static_cast<const float*>(V), static_cast<float*>(O), LSE, sq, status, BH,
+                          d, scale, st) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+  }
+  if (!get_encode_fn()) return FA_ERR_CUDA;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_seq_bf16(&a.tmQ, Q, sq, planes, d, 128) || !encode_seq_bf16(&a.tmK, K, sq, planes, d, 128) ||
+      !encode_seq_bf16(&a.tmV, V, sq, planes, d, 128))
+    return FA_ERR_CUDA;
+  a.O = O;
+  a.LSE = LSE;
+  a.seq = sq;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.wait_limit_ns = kDefaultWaitLimitNs;
+  return launch_fwd_bf16(a, BH, d, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                   void* workspace, size_t workspace_bytes, const SeqArgs& sq, int B, int d,
+                   float scale, fa_dtype dt, void* stream) {
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
+    return FA_ERR_INVALID_ARG;
+  const size_t al = dt == FA_BF16 ? 16 : 4;
+  if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) ||
+      !aligned(dO, al) || !aligned(dQ, al) || !aligned(dK, al) || !aligned(dV, al) ||
+      !aligned(LSE, 4) || !aligned(workspace, 256))
+    return FA_ERR_INVALID_ARG;
+  const BwdWorkspaceLayout L = bwd_layout(sq, B, d, dt);
+  if (workspace_bytes < L.total) return FA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * sq.H;
+  int* status = device_status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  if (dt == FA_F32) {
+    return launch_bwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
+                          static_cast<const float*>(V), static_cast<const float*>(O),
+                          static_cast<const float*>(dO), LSE, static_cast<float*>(dQ),
+                          static_cast<float*>(dK), static_cast<float*>(dV),
+                          static_cast<float*>(workspace), sq, status, BH, d, scale, stages,
+                          st) == cudaSuccess
+               ? FA_OK
+               : FA_ERR_CUDA;
+  }
+  if (!get_encode_fn()) return FA_ERR_CUDA;
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  // query-side tiles (Q, dO) are bwd_query_tile(d) rows, key-side tiles 128 rows
+  const int qrows = bwd_query_tile(d);
+  if (!encode_seq_bf16(&a.tmQ, Q, sq, L.planes, d, qrows) ||
+      !encode_seq_bf16(&a.tmK, K, sq, L.planes, d, 128) ||
+      !encode_seq_bf16(&a.tmV, V, sq, L.planes, d, 128) ||
+      !encode_seq_bf16(&a.tmdO, dO, sq, L.planes, d, qrows))
+    return FA_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  a.O = O;
+  a.dO = dO;
+  a.LSE = LSE;
+  a.dQ = dQ;
+  a.dK = dK;
+  a.dV = dV;
+  a.dQacc = reinterpret_cast<float*>(ws + L.dqacc);
+  if (!encode_acc_f32(&a.tmDQacc, a.dQacc, (long long)L.planes * L.ws_rows, d)) return FA_ERR_CUDA;
+  a.lse2 = reinterpret_cast<float*>(ws + L.lse2);
+  a.Drow = reinterpret_cast<float*>(ws + L.drow);
+  a.seq = sq;
+  a.planes = L.planes;
+  a.ws_rows = L.ws_rows;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.wait_limit_ns = kDefaultWaitLimitNs;
+  return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fa_version(void) { return 100; }
@@ -162,130 +318,85 @@ const char* fa_status_string(fa_status s) {
   }
 }
 
+fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                    int N, int d, float scale, int flags, fa_dtype dt, void* stream) {
+  const fa_status s = check_shape(B, H, N, d, scale, dt);
+  if (s != FA_OK) return s;
+  if (flags & ~FA_CAUSAL) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, fixed_seq(H, N, d, flags & FA_CAUSAL), B, d, scale, dt, stream);
+}
+
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                  int N, int d, float scale, fa_dtype dt, void* stream) {
-  fa_status s = check_shape(B, H, N, d, scale, dt);
+  return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, 0, dt, stream);
+}
+
+fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        const int* cu_seqlens, int B, int H, int total, int max_seqlen, int d,
+                        float scale, int flags, fa_dtype dt, void* stream) {
+  const fa_status s = check_varlen(cu_seqlens, B, H, total, max_seqlen, d, scale, dt);
   if (s != FA_OK) return s;
-  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
-  const size_t al = dt == FA_BF16 ? 16 : 4;
-  if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) || !aligned(LSE, 4))
-    return FA_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
-  if (dt == FA_F32) {
-    return launch_fwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
-                          static_cast<const float*>(V), static_cast<float*>(O), LSE, BH, N, d,
-                          scale, st) == cudaSuccess
-               ? FA_OK
-               : FA_ERR_CUDA;
-  }
-  if (!get_encode_fn()) return FA_ERR_CUDA;
-  int* status = device_status_ptr();
-  if (!status) return FA_ERR_CUDA;
-  FwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!encode_bhnd_bf16(&a.tmQ, Q, BH, N, d, 128) || !encode_bhnd_bf16(&a.tmK, K, BH, N, d, 128) ||
-      !encode_bhnd_bf16(&a.tmV, V, BH, N, d, 128))
-    return FA_ERR_CUDA;
-  a.O = O;
-  a.LSE = LSE;
-  a.N = N;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.status = status;
-  a.wait_limit_ns = kDefaultWaitLimitNs;
-  return launch_fwd_bf16(a, BH, d, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (flags & ~FA_CAUSAL) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, varlen_seq(cu_seqlens, H, total, max_seqlen, d, flags & FA_CAUSAL),
+                  B, d, scale, dt, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt) {
   if (check_shape(B, H, N, d, 1.0f, dt) != FA_OK) return 0;
-  return bwd_layout(B, H, N, d, dt).total;
+  return bwd_layout(fixed_seq(H, N, d, false), B, d, dt).total;
 }
 
-}  // extern "C"
+size_t fa_bwd_varlen_workspace_bytes(int B, int H, int total, int max_seqlen, int d, fa_dtype dt) {
+  static const int kDummy[2] = {0, 0};  // only the sizes are checked here
+  if (check_varlen(kDummy, B, H, total, max_seqlen, d, 1.0f, dt) != FA_OK) return 0;
+  return bwd_layout(varlen_seq(kDummy, H, total, max_seqlen, d, false), B, d, dt).total;
+}
 
-namespace {
-fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V, const void* O,
-                   const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                   void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                   float scale, fa_dtype dt, void* stream) {
-  fa_status s = check_shape(B, H, N, d, scale, dt);
+fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                    size_t workspace_bytes, int B, int H, int N, int d, float scale, int flags,
+                    fa_dtype dt, void* stream) {
+  const fa_status s = check_shape(B, H, N, d, scale, dt);
   if (s != FA_OK) return s;
-  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
-    return FA_ERR_INVALID_ARG;
-  const size_t al = dt == FA_BF16 ? 16 : 4;
-  if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) ||
-      !aligned(dO, al) || !aligned(dQ, al) || !aligned(dK, al) || !aligned(dV, al) ||
-      !aligned(LSE, 4) || !aligned(workspace, 256))
-    return FA_ERR_INVALID_ARG;
-  const BwdWorkspaceLayout L = bwd_layout(B, H, N, d, dt);
-  if (workspace_bytes < L.total) return FA_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
-  if (dt == FA_F32) {
-    return launch_bwd_f32(static_cast<const float*>(Q), static_cast<const float*>(K),
-                          static_cast<const float*>(V), static_cast<const float*>(O),
-                          static_cast<const float*>(dO), LSE, static_cast<float*>(dQ),
-                          static_cast<float*>(dK), static_cast<float*>(dV),
-                          static_cast<float*>(workspace), BH, N, d, scale, stages, st) == cudaSuccess
-               ? FA_OK
-               : FA_ERR_CUDA;
-  }
-  if (!get_encode_fn()) return FA_ERR_CUDA;
-  int* status = device_status_ptr();
-  if (!status) return FA_ERR_CUDA;
-  BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  // query-side tiles (Q, dO) are bwd_query_tile(d) rows, key-side tiles 128 rows
-  const int qrows = bwd_query_tile(d);
-  if (!encode_bhnd_bf16(&a.tmQ, Q, BH, N, d, qrows) || !encode_bhnd_bf16(&a.tmK, K, BH, N, d, 128) ||
-      !encode_bhnd_bf16(&a.tmV, V, BH, N, d, 128) || !encode_bhnd_bf16(&a.tmdO, dO, BH, N, d, qrows))
-    return FA_ERR_CUDA;
-  char* ws = static_cast<char*>(workspace);
-  a.O = O;
-  a.dO = dO;
-  a.LSE = LSE;
-  a.dQ = dQ;
-  a.dK = dK;
-  a.dV = dV;
-  a.dQacc = reinterpret_cast<float*>(ws + L.dqacc);
-  if (!encode_acc_f32(&a.tmDQacc, a.dQacc, (long long)BH * L.Npad, d)) return FA_ERR_CUDA;
-  a.lse2 = reinterpret_cast<float*>(ws + L.lse2);
-  a.Drow = reinterpret_cast<float*>(ws + L.drow);
-  a.N = N;
-  a.Npad = L.Npad;
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.status = status;
-  a.wait_limit_ns = kDefaultWaitLimitNs;
-  return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (flags & ~(FA_CAUSAL | FA_STAGE_MASK)) return FA_ERR_INVALID_ARG;
+  return bwd_impl(flag_stages(flags), Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes,
+                  fixed_seq(H, N, d, flags & FA_CAUSAL), B, d, scale, dt, stream);
 }
-}  // namespace
-
-extern "C" {
 
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                  const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
                  size_t workspace_bytes, int B, int H, int N, int d, float scale, fa_dtype dt,
                  void* stream) {
-  return bwd_impl(kStageAll, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H,
-                  N, d, scale, dt, stream);
+  return fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale,
+                   0, dt, stream);
 }
 
 fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, const void* O,
                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                        void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                        float scale, fa_dtype dt, void* stream) {
-  unsigned bits;
+  int bits;
   switch (stage) {
-    case FA_BWD_PREPROCESS: bits = kStagePre; break;
-    case FA_BWD_MAIN: bits = kStageMain; break;
-    case FA_BWD_DQ_CONVERT: bits = kStageConvert; break;
+    case FA_BWD_PREPROCESS: bits = FA_STAGE_PREPROCESS; break;
+    case FA_BWD_MAIN: bits = FA_STAGE_MAIN; break;
+    case FA_BWD_DQ_CONVERT: bits = FA_STAGE_DQ_CONVERT; break;
     default: return FA_ERR_INVALID_ARG;
   }
-  return bwd_impl(bits, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d,
-                  scale, dt, stream);
+  return fa_bwd_ex(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, scale,
+                   bits, dt, stream);
 }
 
+fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, void* dQ, void* dK, void* dV, const int* cu_seqlens,
+                        void* workspace, size_t workspace_bytes, int B, int H, int total,
+                        int max_seqlen, int d, float scale, int flags, fa_dtype dt, void* stream) {
+  const fa_status s = check_varlen(cu_seqlens, B, H, total, max_seqlen, d, scale, dt);
+  if (s != FA_OK) return s;
+  if (flags & ~(FA_CAUSAL | FA_STAGE_MASK)) return FA_ERR_INVALID_ARG;
+  return bwd_impl(flag_stages(flags), Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes,
+                  varlen_seq(cu_seqlens, H, total, max_seqlen, d, flags & FA_CAUSAL), B, d, scale,
+                  dt, stream);
+}
 
 fa_status fa_softmax_rows(const void* X, void* Y, int rows, int cols, float scale, fa_dtype dt,
                           void* stream) {
@@ -398,7 +509,10 @@ fa_status fa_check_device_status(void* stream) {
   if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
   if (v != 0 && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
     return FA_ERR_CUDA;
-  return v == 0 ? FA_OK : (v == kStatusTimeout ? FA_ERR_TIMEOUT : FA_ERR_CUDA);
+  if (v == 0) return FA_OK;
+  if (v == kStatusTimeout) return FA_ERR_TIMEOUT;
+  if (v == kStatusBadSeqlens) return FA_ERR_INVALID_ARG;
+  return FA_ERR_CUDA;
 }
 
 fa_status fa_debug_timeout_probe(long long limit_ns, void* stream) {

@@ -16,24 +16,44 @@ constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;  // 1 s
 // Device-side status word of the current device (created on first use).
 int* device_status_ptr();
 
+// Where the rows of each (batch, head) live and which keys a query row sees.
+//  * fixed length (cu_seqlens == nullptr): a [B, H, N, d] tensor; (b, h) is
+//    plane b*H + h with rows 0..N-1 (row_stride = d, plane_stride = N*d,
+//    statistics [B*H, N]: stat_plane = N).
+//  * variable length: a packed [total, H, d] tensor; sequence b holds rows
+//    cu_seqlens[b] .. cu_seqlens[b+1]-1 of plane h (row_stride = H*d,
+//    plane_stride = d, statistics [H, total]: stat_plane = total).
+// causal: query row r of a sequence sees keys c <= r of the same sequence.
+struct SeqArgs {
+  const int* cu_seqlens;  // device [B+1] or nullptr
+  int H;
+  int N;                  // fixed length, or the longest sequence (the grid covers it)
+  int total;              // rows per plane of the tensors (fixed: N)
+  int causal;
+  long long row_stride, plane_stride;  // elements
+  long long stat_plane;                // elements between planes of LSE / statistics
+};
+
 // ---- fp32 CUDA-core path (attn_f32.cu) ----
 cudaError_t launch_fwd_f32(const float* Q, const float* K, const float* V, float* O, float* LSE,
-                           int BH, int N, int d, float scale, cudaStream_t st);
+                           const SeqArgs& sq, int* status, int BH, int d, float scale,
+                           cudaStream_t st);
 // Backward stage bits: preprocess, main, dQ convert.
 enum : unsigned { kStagePre = 1u, kStageMain = 2u, kStageConvert = 4u, kStageAll = 7u };
+// Dws: D per row, [planes, total] floats.
 cudaError_t launch_bwd_f32(const float* Q, const float* K, const float* V, const float* O,
                            const float* dO, const float* LSE, float* dQ, float* dK, float* dV,
-                           float* Dws, int BH, int N, int d, float scale, unsigned stages,
-                           cudaStream_t st);
+                           float* Dws, const SeqArgs& sq, int* status, int BH, int d, float scale,
+                           unsigned stages, cudaStream_t st);
 
 // ---- bf16 tcgen05 path ----
-// Tensor maps describe one [BH, N, d] bf16 tensor as 3-D (d, N, BH) with
-// 64-element x 128-row boxes and 128-byte swizzle.
+// Tensor maps view a bf16 tensor of the SeqArgs layout as 3-D (d, rows,
+// planes) with 64-element x {128, 64}-row boxes and 128-byte swizzle.
 struct FwdArgs {
-  CUtensorMap tmQ, tmK, tmV;
-  void* O;      // bf16 [BH, N, d]
-  float* LSE;   // [BH, N]
-  int N;
+  CUtensorMap tmQ, tmK, tmV;  // 3-D (d, rows, planes) views of the SeqArgs layout
+  void* O;      // bf16, SeqArgs layout
+  float* LSE;   // SeqArgs statistics layout
+  SeqArgs seq;
   float scale_log2;  // scale * log2(e)
   int* status;
   unsigned long long wait_limit_ns;
@@ -41,25 +61,29 @@ struct FwdArgs {
 cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st);
 
 struct BwdArgs {
-  CUtensorMap tmQ, tmK, tmV, tmdO;
-  CUtensorMap tmDQacc;  // fp32 [BH*Npad, d], 32 x 32 boxes, no swizzle (d = 128 only)
-  const void* O;     // bf16 [BH, N, d]
-  const void* dO;    // bf16 [BH, N, d]
-  const float* LSE;  // [BH, N]
-  void* dQ;          // bf16 [BH, N, d]
-  void* dK;          // bf16 [BH, N, d]
-  void* dV;          // bf16 [BH, N, d]
-  float* dQacc;      // fp32 [BH, Npad, d]
-  float* lse2;       // fp32 [BH, Npad]  LSE * log2(e); +inf past N
-  float* Drow;       // fp32 [BH, Npad]  rowsum(dO o O); 0 past N
-  int N, Npad;
+  CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D (d, rows, planes) views of the SeqArgs layout
+  CUtensorMap tmDQacc;  // fp32 [planes*ws_rows, d], 32 x 32 boxes, no swizzle (d = 128 only)
+  const void* O;     // bf16, SeqArgs layout (as Q, K, V, dO, dQ, dK, dV)
+  const void* dO;
+  const float* LSE;  // SeqArgs statistics layout
+  void* dQ;
+  void* dK;
+  void* dV;
+  float* dQacc;      // fp32 [planes, ws_rows, d]
+  float* lse2;       // fp32 [planes, ws_rows]  -LSE * log2(e); -inf past the rows
+  float* Drow;       // fp32 [planes, ws_rows]  -rowsum(dO o O); 0 past the rows
+  SeqArgs seq;
+  int planes;        // B*H (fixed) or H (variable length)
+  int ws_rows;       // workspace rows per plane, a multiple of 128: roundup(N, 128)
+                     // (fixed length) or roundup(total, 128) + 128 (variable length)
   float scale;
   float scale_log2;
   int* status;
   unsigned long long wait_limit_ns;
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
-// Row padding used by the bf16 backward workspace.
+// Row padding used by the bf16 backward workspace: ws_rows = roundup(total, 128)
+// (+128 with variable lengths, where a sequence's last tile may start anywhere).
 constexpr int kBwdRowPad = 128;
 // Query rows per streamed tile of the bf16 backward kernel (its Q/dO TMA box
 // height); must match BwdCfg<d>::BQ.

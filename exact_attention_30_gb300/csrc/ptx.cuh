@@ -16,7 +16,8 @@ namespace fa {
 // ----------------------------------------------------------------------------
 // status word + bounded waits
 // ----------------------------------------------------------------------------
-enum : int { kStatusOk = 0, kStatusTimeout = 4 };
+// status codes (kStatusBadSeqlens equals FA_ERR_INVALID_ARG, kStatusTimeout FA_ERR_TIMEOUT)
+enum : int { kStatusOk = 0, kStatusBadSeqlens = 1, kStatusTimeout = 4 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

@@ -158,3 +158,17 @@ def decode_inputs(w: DecodeWorkload, seed: int = 0):
     q, k, v, _ = random_qkv(w.B, w.H, w.Nq, w.d, torch.bfloat16, seed=seed, with_do=False,
                             big_key_every=64, n_k=w.Nk)
     return q, k, v
+
+
+def random_varlen(lens, H, d, dtype=torch.bfloat16, seed=0, with_do=True):
+    """Packed variable-length batch: (q, k, v, do, cu_seqlens) with tensors
+    [total, H, d] drawn like ``random_qkv`` (order Q, K, V, dO) and
+    cu_seqlens int32 [len(lens) + 1] (prefix sums of ``lens``), all on the CPU."""
+    g = torch.Generator().manual_seed(seed)
+    total = int(sum(lens))
+    draw = lambda: torch.randn((total, H, d), generator=g, dtype=torch.float32).to(dtype)
+    q, k, v = draw(), draw(), draw()
+    do = draw() if with_do else None
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return q, k, v, do, cu

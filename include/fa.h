@@ -23,7 +23,8 @@
  *    launched", not "finished".
  *  - No call throws; errors are returned as fa_status. Arguments are validated
  *    before anything is launched: on any error nothing is enqueued.
- *  - Attention is non-causal, without mask or dropout.
+ *  - Attention is non-causal, without mask or dropout, unless an _ex or
+ *    _varlen entry point is given FA_CAUSAL.
  *
  * dtypes and head sizes
  *  - FA_BF16: bf16 Q/K/V/O/dO/dQ/dK/dV, float32 accumulation, d in {64, 128}.
@@ -65,6 +66,47 @@ typedef enum { FA_F32 = 0, FA_BF16 = 1 } fa_dtype;
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
                  int B, int H, int N, int d, float scale, fa_dtype dt, void* stream);
 
+/* Flags of the _ex and _varlen entry points. */
+#define FA_CAUSAL 1 /* query row r attends to keys c <= r of its own sequence */
+/* Backward stages (fa_bwd_ex / fa_bwd_varlen); no stage bit = all three, in order. */
+#define FA_STAGE_PREPROCESS (1 << 8)
+#define FA_STAGE_MAIN (2 << 8)
+#define FA_STAGE_DQ_CONVERT (4 << 8)
+#define FA_STAGE_MASK (7 << 8)
+
+/*
+ * fa_fwd with flags: 0 or FA_CAUSAL. Causal attention is not on the source
+ * pages; it is the plainest adjacent variant of the definition for
+ * self-attention: row r of softmax(scale * Q K^T) is taken over keys
+ * c <= r only (the others get weight 0), O and LSE defined over those keys.
+ * Query tiles skip key tiles past their diagonal. Errors: as fa_fwd, plus
+ * FA_ERR_INVALID_ARG for unknown flags.
+ */
+fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    int B, int H, int N, int d, float scale, int flags, fa_dtype dt, void* stream);
+
+/*
+ * Variable-length batch (packed layout, no padding): B sequences of
+ * different lengths, sequence b holding rows cu_seqlens[b] ..
+ * cu_seqlens[b+1]-1 of the packed tensors. Each sequence is attended to
+ * separately (keys of other sequences get weight 0); with FA_CAUSAL row r
+ * of a sequence sees its keys 0..r.
+ *   Q, K, V, O : [total, H, d] (rows of all sequences back to back, then
+ *                heads, d fastest), dtype `dt`.
+ *   LSE        : [H, total] float32 output.
+ *   cu_seqlens : DEVICE int32 [B+1], cu_seqlens[0] = 0, non-decreasing,
+ *                cu_seqlens[B] = total; every length <= max_seqlen <= total
+ *                (max_seqlen sizes the grid). The kernels check each pair:
+ *                a sequence whose offsets break these rules is skipped
+ *                (nothing of it is read or written) and fa_check_device_status
+ *                then returns FA_ERR_INVALID_ARG.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (as fa_fwd; H*total*d <
+ * 2^31, B*H <= 65535), FA_ERR_CUDA.
+ */
+fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        const int* cu_seqlens, int B, int H, int total, int max_seqlen, int d,
+                        float scale, int flags, fa_dtype dt, void* stream);
+
 /*
  * Bytes of device scratch that fa_bwd needs for this problem (0 on invalid
  * arguments). The caller allocates it; its contents on entry do not matter.
@@ -105,6 +147,33 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for an unknown stage.
  */
 typedef enum { FA_BWD_PREPROCESS = 0, FA_BWD_MAIN = 1, FA_BWD_DQ_CONVERT = 2 } fa_bwd_stage_id;
+
+/*
+ * fa_bwd with flags: FA_CAUSAL and/or stage bits (FA_STAGE_PREPROCESS,
+ * FA_STAGE_MAIN, FA_STAGE_DQ_CONVERT; none = all three). The workspace is the
+ * same as fa_bwd's. Pass the flags given to fa_fwd_ex. With FA_CAUSAL the
+ * gradients are those of the causal definition: P is zero above the
+ * diagonal, so key tiles skip the query tiles before their diagonal.
+ * Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for unknown flags.
+ */
+fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                    size_t workspace_bytes, int B, int H, int N, int d, float scale, int flags,
+                    fa_dtype dt, void* stream);
+
+/* Scratch bytes for fa_bwd_varlen (0 on invalid sizes). */
+size_t fa_bwd_varlen_workspace_bytes(int B, int H, int total, int max_seqlen, int d, fa_dtype dt);
+
+/*
+ * Backward pass of fa_fwd_varlen: same packed layout ([total, H, d] tensors,
+ * LSE [H, total], device cu_seqlens), flags and stage bits as fa_bwd_ex,
+ * workspace of >= fa_bwd_varlen_workspace_bytes() bytes, 256-byte aligned.
+ * Errors: as fa_fwd_varlen, plus FA_ERR_INVALID_ARG for a small workspace.
+ */
+fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, void* dQ, void* dK, void* dV, const int* cu_seqlens,
+                        void* workspace, size_t workspace_bytes, int B, int H, int total,
+                        int max_seqlen, int d, float scale, int flags, fa_dtype dt, void* stream);
 
 fa_status fa_bwd_stage(int stage, const void* Q, const void* K, const void* V, const void* O,
                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
@@ -194,7 +263,9 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device. Returns FA_ERR_TIMEOUT if any kernel launched
  * since the last check abandoned a bounded wait (its outputs are then
- * undefined), FA_ERR_CUDA if the stream reports an error, FA_OK otherwise.
+ * undefined), FA_ERR_INVALID_ARG if a variable-length call met inconsistent
+ * cu_seqlens (the sequences concerned were skipped), FA_ERR_CUDA if the
+ * stream reports an error, FA_OK otherwise.
  */
 fa_status fa_check_device_status(void* stream);
 

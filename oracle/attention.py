@@ -37,6 +37,15 @@ library primitive used as a step):
   problem (N_q new queries, N_k cached keys); the split form is checked
   against it.
 
+* ``causal=True`` (every function above that takes it) -- not on the pages:
+  the plainest adjacent variant of the definition for self-attention. Score
+  S_rc of query row r and key c is kept only for c <= r; the others are set
+  to -inf before the softmax, so P_rc = 0 there and the backward formulas
+  above need no change (dS = 0 where P = 0).
+* ``varlen_attention_fwd`` / ``varlen_attention_bwd`` -- a packed batch of
+  sequences of different lengths ([total, H, d], offsets cu_seqlens): each
+  sequence and head is attended to on its own, by the functions above.
+
 Readings where the pages are silent (each also listed in the design notes):
 * ``scale`` is a free argument; the pages fix 1/sqrt(d). dS carries exactly one
   factor of ``scale`` (the pages' "/ sqrt(d)" in the dS line).
@@ -66,6 +75,9 @@ __all__ = [
     "attention_bwd_batched",
     "merge_partials",
     "split_kv_attention_fwd",
+    "causal_mask",
+    "varlen_attention_fwd",
+    "varlen_attention_bwd",
 ]
 
 
@@ -73,13 +85,25 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def scores(Q, K, scale: float) -> np.ndarray:
-    """S = scale * Q K^T, materialised (N_q x N_k).
+def causal_mask(n_q: int, n_k: int, rows=None) -> np.ndarray:
+    """Boolean [n_q, n_k]: True where key c is visible to query row r (c <= r).
+
+    ``rows``: the global row indices of the n_q query rows (default 0..n_q-1).
+    """
+    r = np.arange(n_q) if rows is None else np.asarray(rows, dtype=np.int64)
+    return np.arange(n_k)[None, :] <= r[:, None]
+
+
+def scores(Q, K, scale: float, causal: bool = False, rows=None) -> np.ndarray:
+    """S = scale * Q K^T, materialised (N_q x N_k); -inf where a causal mask hides a key.
 
     "Lesson 1: FlashAttention core idea" §1 (the formula and the explicit
     intermediate matrices); "Interview Q15" Step 1.
     """
-    return float(scale) * (_f64(Q) @ _f64(K).T)
+    S = float(scale) * (_f64(Q) @ _f64(K).T)
+    if causal:
+        S = np.where(causal_mask(S.shape[0], S.shape[1], rows), S, -np.inf)
+    return S
 
 
 def row_softmax(S):
@@ -97,33 +121,33 @@ def row_softmax(S):
     return P, m, l
 
 
-def attention_fwd(Q, K, V, scale: float):
+def attention_fwd(Q, K, V, scale: float, causal: bool = False, rows=None):
     """Exact attention forward for one head: (O, LSE).
 
     O = softmax(scale * Q K^T) V ("Lesson 1" §1; "Interview Q15" Steps 1-3;
     "FlashAttention and Triton" §19.2). LSE_r = m_r + ln(l_r): the per-row
     statistics that "Lesson 1" §5 keeps for the backward pass, folded into one
     number.
-    Q: [N_q, d], K: [N_k, d], V: [N_k, d_v].
+    Q: [N_q, d], K: [N_k, d], V: [N_k, d_v]. ``causal``/``rows``: see ``scores``.
     """
-    S = scores(Q, K, scale)
+    S = scores(Q, K, scale, causal, rows)
     P, m, l = row_softmax(S)
     O = P @ _f64(V)
     LSE = m + np.log(l)
     return O, LSE
 
 
-def attention_fwd_rows(Q, K, V, scale: float, rows):
+def attention_fwd_rows(Q, K, V, scale: float, rows, causal: bool = False):
     """The definition of ``attention_fwd`` evaluated for the query rows ``rows`` only.
 
     Softmax is row-local ("FlashAttention and Triton" §19.11: one program per
     row), so row r of O and LSE depends only on query row r and all of K, V.
     """
     rows = np.asarray(rows, dtype=np.int64)
-    return attention_fwd(_f64(Q)[rows], K, V, scale)
+    return attention_fwd(_f64(Q)[rows], K, V, scale, causal, rows)
 
 
-def attention_bwd(Q, K, V, dO, scale: float):
+def attention_bwd(Q, K, V, dO, scale: float, causal: bool = False):
     """Exact attention backward for one head: (dQ, dK, dV).
 
     "Lesson 1: FlashAttention core idea" §5, written for whole matrices:
@@ -137,7 +161,7 @@ def attention_bwd(Q, K, V, dO, scale: float):
     loop; only the full-row sum is the gradient of softmax).
     """
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
-    S = scores(Q, K, scale)
+    S = scores(Q, K, scale, causal)
     P, _, _ = row_softmax(S)
     dV = P.T @ dO
     dP = dO @ V.T
@@ -204,7 +228,7 @@ def online_softmax_stats(blocks):
     return out
 
 
-def attention_fwd_batched(Q, K, V, scale: float, heads=None):
+def attention_fwd_batched(Q, K, V, scale: float, heads=None, causal: bool = False):
     """``attention_fwd`` applied to every (b, h) of [B, H, N, d] arrays.
 
     ``heads``: optional list of (b, h) pairs to compute; others stay NaN.
@@ -215,11 +239,11 @@ def attention_fwd_batched(Q, K, V, scale: float, heads=None):
     O = np.full((B, H, N, V.shape[-1]), np.nan)
     LSE = np.full((B, H, N), np.nan)
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
-        O[b, h], LSE[b, h] = attention_fwd(Q[b, h], K[b, h], V[b, h], scale)
+        O[b, h], LSE[b, h] = attention_fwd(Q[b, h], K[b, h], V[b, h], scale, causal)
     return O, LSE
 
 
-def attention_bwd_batched(Q, K, V, dO, scale: float, heads=None):
+def attention_bwd_batched(Q, K, V, dO, scale: float, heads=None, causal: bool = False):
     """``attention_bwd`` applied to every (b, h) of [B, H, N, d] arrays.
 
     ``heads``: optional list of (b, h) pairs to compute; others stay NaN.
@@ -230,7 +254,8 @@ def attention_bwd_batched(Q, K, V, dO, scale: float, heads=None):
     dK = np.full(K.shape, np.nan)
     dV = np.full(V.shape, np.nan)
     for b, h in (heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]):
-        dQ[b, h], dK[b, h], dV[b, h] = attention_bwd(Q[b, h], K[b, h], V[b, h], dO[b, h], scale)
+        dQ[b, h], dK[b, h], dV[b, h] = attention_bwd(Q[b, h], K[b, h], V[b, h], dO[b, h], scale,
+                                                     causal)
     return dQ, dK, dV
 
 
@@ -262,3 +287,35 @@ def split_kv_attention_fwd(Q, K, V, scale: float, keys_per_split: int):
     k = int(keys_per_split)
     parts = [attention_fwd(Q, K[s:s + k], V[s:s + k], scale) for s in range(0, K.shape[0], k)]
     return merge_partials([p[0] for p in parts], [p[1] for p in parts])
+
+
+def varlen_attention_fwd(Q, K, V, cu_seqlens, scale: float, causal: bool = False):
+    """Packed variable-length batch: Q, K, V [total, H, d]; sequence b is rows
+    cu_seqlens[b]..cu_seqlens[b+1]-1. Returns O [total, H, d_v], LSE [H, total]."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    cu = [int(x) for x in cu_seqlens]
+    total, H = Q.shape[:2]
+    O = np.full((total, H, V.shape[-1]), np.nan)
+    LSE = np.full((H, total), np.nan)
+    for b in range(len(cu) - 1):
+        s, e = cu[b], cu[b + 1]
+        if e == s:
+            continue
+        for h in range(H):
+            O[s:e, h], LSE[h, s:e] = attention_fwd(Q[s:e, h], K[s:e, h], V[s:e, h], scale, causal)
+    return O, LSE
+
+
+def varlen_attention_bwd(Q, K, V, dO, cu_seqlens, scale: float, causal: bool = False):
+    """Backward of ``varlen_attention_fwd``: dQ, dK, dV [total, H, d]."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    cu = [int(x) for x in cu_seqlens]
+    dQ, dK, dV = np.zeros(Q.shape), np.zeros(K.shape), np.zeros(V.shape)
+    for b in range(len(cu) - 1):
+        s, e = cu[b], cu[b + 1]
+        if e == s:
+            continue
+        for h in range(Q.shape[1]):
+            dQ[s:e, h], dK[s:e, h], dV[s:e, h] = attention_bwd(Q[s:e, h], K[s:e, h], V[s:e, h],
+                                                              dO[s:e, h], scale, causal)
+    return dQ, dK, dV

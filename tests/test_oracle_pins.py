@@ -14,7 +14,7 @@ import torch
 
 from oracle import (attention_bwd, attention_fwd, attention_fwd_rows, merge_partials,
                     online_softmax_stats, row_softmax, scores, split_kv_attention_fwd,
-                    tiled_attention_fwd)
+                    tiled_attention_fwd, varlen_attention_bwd, varlen_attention_fwd)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -293,3 +293,102 @@ def test_merge_of_a_dominant_range_returns_it():
     O_a, O_b = np.full((1, 2), 3.0), np.full((1, 2), -5.0)
     O, L = merge_partials([O_a, O_b], [np.array([800.0]), np.array([0.0])])
     assert np.allclose(O, 3.0, rtol=0, atol=1e-300) and abs(L[0] - 800.0) < 1e-12
+
+
+# ---------------------------------------------------------------- causal and variable length
+def test_causal_against_brute_force_loops():
+    """Pure-Python loops over visible keys only (c <= r), math.exp / math.log."""
+    rng = np.random.default_rng(77)
+    n, d, scale = 6, 3, 0.7
+    Q, K, V = rng.normal(size=(n, d)), rng.normal(size=(n, d)), rng.normal(size=(n, d))
+    O, LSE = attention_fwd(Q, K, V, scale, causal=True)
+    for r in range(n):
+        s = [scale * sum(Q[r, i] * K[c, i] for i in range(d)) for c in range(r + 1)]
+        m = max(s)
+        w = [math.exp(x - m) for x in s]
+        l = sum(w)
+        for j in range(d):
+            assert abs(O[r, j] - sum(w[c] * V[c, j] for c in range(r + 1)) / l) < 1e-14
+        assert abs(LSE[r] - (m + math.log(l))) < 1e-14
+
+
+def test_causal_closed_forms():
+    """Row 0 sees only key 0 (O_0 = V_0, LSE_0 = scale q_0.k_0); the last row
+    sees every key (equal to the non-causal last row)."""
+    rng = np.random.default_rng(78)
+    Q, K, V = rng.normal(size=(9, 5)), rng.normal(size=(9, 5)), rng.normal(size=(9, 4))
+    O, LSE = attention_fwd(Q, K, V, 0.4, causal=True)
+    assert np.abs(O[0] - V[0]).max() < 1e-15 and abs(LSE[0] - 0.4 * Q[0] @ K[0]) < 1e-14
+    O2, LSE2 = attention_fwd(Q, K, V, 0.4)
+    assert np.abs(O[-1] - O2[-1]).max() < 1e-14 and abs(LSE[-1] - LSE2[-1]) < 1e-14
+    rows = np.array([8, 0, 4])
+    Or, Lr = attention_fwd_rows(Q, K, V, 0.4, rows, causal=True)
+    assert np.abs(Or - O[rows]).max() < 1e-15 and np.abs(Lr - LSE[rows]).max() < 1e-15
+
+
+@pytest.mark.parametrize("n", [1, 7, 33])
+def test_causal_against_torch_sdpa_and_autograd_float64(n):
+    B, H, d = 1, 2, 8
+    g = torch.Generator().manual_seed(n)
+    q, k, v = (torch.randn(B, H, n, d, dtype=torch.float64, generator=g, requires_grad=True)
+               for _ in range(3))
+    do = torch.randn(B, H, n, d, dtype=torch.float64, generator=g)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    o.backward(do)
+    s = 1 / math.sqrt(d)
+    for h in range(H):
+        Q, K, V, dO = (t[0, h].detach().numpy() for t in (q, k, v, do))
+        O, _ = attention_fwd(Q, K, V, s, causal=True)
+        assert np.abs(O - o[0, h].detach().numpy()).max() <= 1e-12
+        dQ, dK, dV = attention_bwd(Q, K, V, dO, s, causal=True)
+        for mine, ref in ((dQ, q.grad), (dK, k.grad), (dV, v.grad)):
+            assert np.abs(mine - ref[0, h].numpy()).max() <= 1e-12
+
+
+def test_causal_backward_against_central_differences():
+    rng = np.random.default_rng(5)
+    N, d, h = 4, 3, 1e-6
+    Q, K, V, G = (rng.normal(size=(N, d)) for _ in range(4))
+
+    def loss(Q_, K_, V_):
+        return float((attention_fwd(Q_, K_, V_, 0.6, causal=True)[0] * G).sum())
+
+    grads = attention_bwd(Q, K, V, G, 0.6, causal=True)
+    for which, dX in enumerate(grads):
+        X = (Q, K, V)[which]
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            args_p, args_m = [Q.copy(), K.copy(), V.copy()], [Q.copy(), K.copy(), V.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.abs(num - dX).max() / max(np.abs(dX).max(), 1e-300) <= 1e-7
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_against_torch_sdpa_per_sequence(causal):
+    """A packed batch equals independent attention per sequence (torch float64)."""
+    lens = [5, 1, 12, 0, 7]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    total, H, d = int(cu[-1]), 3, 4
+    g = torch.Generator().manual_seed(3)
+    q, k, v, do = (torch.randn(total, H, d, dtype=torch.float64, generator=g) for _ in range(4))
+    O, LSE = varlen_attention_fwd(q.numpy(), k.numpy(), v.numpy(), cu, 0.5, causal)
+    dQ, dK, dV = varlen_attention_bwd(q.numpy(), k.numpy(), v.numpy(), do.numpy(), cu, 0.5, causal)
+    for b in range(len(lens)):
+        s, e = int(cu[b]), int(cu[b + 1])
+        if s == e:
+            continue
+        qs, ks, vs = (t[s:e].transpose(0, 1).clone().requires_grad_(True) for t in (q, k, v))
+        o = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, scale=0.5, is_causal=causal)
+        o.backward(do[s:e].transpose(0, 1))
+        assert np.abs(O[s:e] - o.detach().transpose(0, 1).numpy()).max() <= 1e-12
+        for mine, ref in ((dQ, qs.grad), (dK, ks.grad), (dV, vs.grad)):
+            assert np.abs(mine[s:e] - ref.transpose(0, 1).numpy()).max() <= 1e-12
+        # LSE from its definition: log of the sum of exp over the visible scores
+        for h in range(H):
+            S = 0.5 * q[s:e, h].numpy() @ k[s:e, h].numpy().T
+            if causal:
+                S = np.where(np.tril(np.ones_like(S, dtype=bool)), S, -np.inf)
+            ref_lse = np.log(np.exp(S - S.max(1, keepdims=True)).sum(1)) + S.max(1)
+            assert np.abs(LSE[h, s:e] - ref_lse).max() <= 1e-12

@@ -14,7 +14,9 @@ import torch
 import exact_attention_30_gb300 as fa
 from exact_attention_30_gb300.inputs import WORKLOADS, random_qkv, workload_inputs
 from oracle import attention_bwd
-from parity_utils import TOL_BF16_GRAD, rel_max, to64
+import numpy as np
+
+from parity_utils import TOL_BF16_GRAD, grad_within, rel_max, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -32,9 +34,9 @@ def _check_heads(q, k, v, do, grads, scale, heads):
     g64 = [to64(g) for g in grads]
     for b, h in heads:
         ref = attention_bwd(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale)
+        cancel = float(np.abs(do64[b, h]).max() * np.abs(v64[b, h]).max() * q64.shape[-1])
         for name, got, r in zip(("dQ", "dK", "dV"), g64, ref):
-            err = rel_max(got[b, h], r)
-            assert err <= TOL_BF16_GRAD, (name, b, h, err)
+            assert grad_within(got[b, h], r, cancel), (name, b, h, rel_max(got[b, h], r))
 
 
 @pytest.mark.parametrize("N", [1, 17, 64, 65, 128, 129, 200, 257, 1000])
