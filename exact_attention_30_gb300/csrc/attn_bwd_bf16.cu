@@ -291,9 +291,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ producer: stats, dO ring
-    // The whole warp copies each query tile's two statistics rows (lane k
-    // takes rows 4k..4k+3; a sequence may start at any row, so these are
-    // plain loads) and lane 0 issues the dO tile loads.
+    // Each query tile's two statistics rows: with the fixed-length layout one
+    // bulk copy each (rows past N hold the neutral padding); in a packed
+    // batch, where a sequence may start at any row and the tile's last rows
+    // may belong to the next sequence, the whole warp copies them with plain
+    // loads (lane k: rows 4k..4k+3) and sets -LSE*log2e = -inf past the
+    // sequence, so that P = 0 there. Lane 0 issues the dO tile loads.
+    const bool stat_bulk = a.seq.cu_seqlens == nullptr;  // rows 16-byte aligned, padded
     if (lane == 0) tma_prefetch_desc(&a.tmdO);
     int last = -1;  // lane 0: last dO tile issued
     for (int i = 0; i < n_it; ++i) {
@@ -305,14 +309,29 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           if (lane == 0) *abort_flag = 1;
           break;
         }
-        const size_t row0 = ws_row0 + (size_t)(i_begin + i) * C::BQ + 4 * lane;
-        float* dst = reinterpret_cast<float*>(smem + C::OFF_STAT + t * C::STAT_BYTES) + 4 * lane;
-        const float4 l4 = make_float4(a.lse2[row0], a.lse2[row0 + 1], a.lse2[row0 + 2], a.lse2[row0 + 3]);
-        const float4 d4 = make_float4(a.Drow[row0], a.Drow[row0 + 1], a.Drow[row0 + 2], a.Drow[row0 + 3]);
-        *reinterpret_cast<float4*>(dst) = l4;
-        *reinterpret_cast<float4*>(dst + C::BQ) = d4;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_STFULL + t));
+        const int q_row = (i_begin + i) * C::BQ;  // first query row of the tile, within the sequence
+        if (stat_bulk) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(BAR(B_STFULL + t), C::STAT_BYTES);
+            bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES, a.lse2 + ws_row0 + q_row, C::BQ * 4,
+                      BAR(B_STFULL + t));
+            bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES + C::BQ * 4, a.Drow + ws_row0 + q_row,
+                      C::BQ * 4, BAR(B_STFULL + t));
+          }
+        } else {
+          const size_t row0 = ws_row0 + (size_t)q_row + 4 * lane;
+          const int live = N - q_row - 4 * lane;  // rows of this lane inside the sequence
+          float* dst = reinterpret_cast<float*>(smem + C::OFF_STAT + t * C::STAT_BYTES) + 4 * lane;
+          const float4 l4 = make_float4(live > 0 ? a.lse2[row0] : -INFINITY,
+                                        live > 1 ? a.lse2[row0 + 1] : -INFINITY,
+                                        live > 2 ? a.lse2[row0 + 2] : -INFINITY,
+                                        live > 3 ? a.lse2[row0 + 3] : -INFINITY);
+          const float4 d4 = make_float4(a.Drow[row0], a.Drow[row0 + 1], a.Drow[row0 + 2], a.Drow[row0 + 3]);
+          *reinterpret_cast<float4*>(dst) = l4;
+          *reinterpret_cast<float4*>(dst + C::BQ) = d4;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_STFULL + t));
+        }
       }
       if (lane == 0) {
         const int s = i % C::DOSTAGES;
@@ -460,12 +479,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     for (int i = 0; i < n_it; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       const int st = i % C::STATSTAGES;
-      const int qi = i_begin + i;  // query tile
-      // columns q of this tile with P = 0: q >= q_end (past the sequence) and,
-      // on the causal diagonal, q < r (key r after query q)
-      const int q_end = N - qi * C::BQ;
-      const int q_min = (causal && qi == kb) ? r : 0;
-      const bool mask_cols = q_end < C::BQ || (causal && qi == kb);
+      // On the causal diagonal, P = 0 in the columns q < r (key r after query
+      // q): column 32h + 4k4 + e of this group is masked when it is below
+      // r - 64g. (Queries past the sequence have -LSE*log2e = -inf: P = 0.)
+      const bool diag = causal && i_begin + i == kb;
+      const int r_rel = r - qc0;
       bool w = mbar_wait(BAR(B_SFULL), i & 1, a.status, a.wait_limit_ns) &&
                mbar_wait(BAR(B_STFULL + st), (i / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -488,12 +506,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           const float2 xb = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4 + 2]), __uint_as_float(sr[4 * k4 + 3])), c22, f2_pack(nl.z, nl.w)));
           float p0 = ex2_approx(xa.x), p1 = ex2_approx(xa.y), p2 = ex2_approx(xb.x), p3 = ex2_approx(xb.y);
           if (!key_live) p0 = p1 = p2 = p3 = 0.f;
-          if (mask_cols) {
-            const int q = qc0 + 32 * h + 4 * k4;
-            p0 = (q < q_min || q >= q_end) ? 0.f : p0;
-            p1 = (q + 1 < q_min || q + 1 >= q_end) ? 0.f : p1;
-            p2 = (q + 2 < q_min || q + 2 >= q_end) ? 0.f : p2;
-            p3 = (q + 3 < q_min || q + 3 >= q_end) ? 0.f : p3;
+          if (diag) {
+            const int c = 32 * h + 4 * k4;
+            p0 = c < r_rel ? 0.f : p0;
+            p1 = c + 1 < r_rel ? 0.f : p1;
+            p2 = c + 2 < r_rel ? 0.f : p2;
+            p3 = c + 3 < r_rel ? 0.f : p3;
           }
           pb[16 * h + 2 * k4] = pack_bf16x2(p0, p1);
           pb[16 * h + 2 * k4 + 1] = pack_bf16x2(p2, p3);
