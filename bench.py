@@ -59,6 +59,8 @@ def parse_args():
                         "HBM-bound; not the headline line)")
     p.add_argument("--decode-workload", default="decode_bf16_8x32x1x32768x128",
                    help="named decode workload for --op decode")
+    p.add_argument("--decode-shape", type=int, nargs=5, metavar=("B", "H", "NQ", "NK", "D"),
+                   default=None, help="another decode shape (profiling captures); the JSON line names it")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "f32"],
                    help="element type for --op softmax")
     p.add_argument("--causal", action="store_true",
@@ -527,6 +529,10 @@ def run_decode(args):
     from exact_attention_30_gb300.inputs import DECODE_WORKLOADS, decode_inputs
 
     w = DECODE_WORKLOADS[args.decode_workload]
+    if args.decode_shape is not None:
+        from exact_attention_30_gb300.inputs import DecodeWorkload
+        b_, h_, nq_, nk_, d_ = args.decode_shape
+        w = DecodeWorkload(f"decode_bf16_{b_}x{h_}x{nq_}x{nk_}x{d_}", b_, h_, nq_, nk_, d_)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     fa.load_library()
