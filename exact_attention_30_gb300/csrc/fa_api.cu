@@ -453,8 +453,9 @@ fa_status fa_decode_plan(int B, int H, int Nq, int Nk, int d, int resident_ctas,
   if (!splits || !keys_per_split || resident_ctas < 0) return FA_ERR_INVALID_ARG;
   const fa_status s = check_decode(B, H, Nq, Nk, d, FA_BF16);
   if (s != FA_OK) return s;
-  const DecodePlan p = resident_ctas > 0 ? plan_decode_for_slots(B * H, Nk, resident_ctas)
-                                         : plan_decode(B * H, Nq, Nk, d);
+  const DecodePlan p = resident_ctas > 0
+                           ? plan_decode_for_slots(B * H, Nk, resident_ctas, decode_tile_keys(Nq))
+                           : plan_decode(B * H, Nq, Nk, d);
   if (p.splits < 1) return FA_ERR_CUDA;
   *splits = p.splits;
   *keys_per_split = p.keys_per_split;
@@ -480,7 +481,10 @@ fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float*
   const int BH = B * H;
   DecodeArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_bhnd_bf16(&a.tmK, K, BH, Nk, d, 64) || !encode_bhnd_bf16(&a.tmV, V, BH, Nk, d, 64))
+  // TMA boxes are the decode kernel's key tile (64 or 128 rows)
+  const int box_rows = decode_tile_keys(Nq);
+  if (!encode_bhnd_bf16(&a.tmK, K, BH, Nk, d, box_rows) ||
+      !encode_bhnd_bf16(&a.tmV, V, BH, Nk, d, box_rows))
     return FA_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   a.Q = Q;

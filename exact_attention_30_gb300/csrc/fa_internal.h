@@ -95,10 +95,10 @@ cudaError_t launch_softmax_rows(const void* X, void* Y, int rows, int cols, floa
                                 cudaStream_t st);
 
 // ---- KV-cache decode (decode_splitkv.cu) ----
-constexpr int kDecodeMaxQueries = 8;
+constexpr int kDecodeMaxQueries = 16;
 constexpr int kDecodeMaxSplits = 256;
 struct DecodeArgs {
-  CUtensorMap tmK, tmV;  // [BH, Nk, d] bf16 as 3-D (d, Nk, BH), 64 x 64 boxes, 128-byte swizzle
+  CUtensorMap tmK, tmV;  // [BH, Nk, d] bf16 as 3-D (d, Nk, BH), 64 x decode_tile_keys(Nq) boxes, 128-byte swizzle
   const void* Q;         // bf16 [BH, Nq, d]
   void* O;               // bf16 [BH, Nq, d]
   float* LSE;            // [BH, Nq], natural log
@@ -116,8 +116,12 @@ struct DecodePlan {
 // Split count for a problem on the current device (queries its SM count and
 // the kernel's occupancy once per device).
 DecodePlan plan_decode(int BH, int Nq, int Nk, int d);
-// The same choice for a given number of resident CTAs on the GPU.
-DecodePlan plan_decode_for_slots(int BH, int Nk, int slots);
+// The same choice for a given number of resident CTAs on the GPU, with key
+// ranges in multiples of `tile` keys.
+DecodePlan plan_decode_for_slots(int BH, int Nk, int slots, int tile);
+// Keys per tile of the decode kernel used for Nq queries per head (64 on CUDA
+// cores for one query, 128 on tensor cores for more).
+int decode_tile_keys(int Nq);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, int d, cudaStream_t st);
 
 // Bounded-wait probe (fa_debug_timeout_probe).

@@ -210,10 +210,12 @@ fa_status fa_softmax_rows(const void* X, void* Y, int rows, int cols, float scal
  *   workspace : device scratch of >= fa_decode_workspace_bytes() bytes,
  *          256-byte aligned, not used by another call in flight; contents on
  *          entry do not matter (split outputs and log-sum-exps, fp32).
- *   dt   : FA_BF16 only; d in {64, 128}; 1 <= Nq <= 8; 1 <= Nk <= 2^30;
+ *   dt   : FA_BF16 only; d in {64, 128}; 1 <= Nq <= 16; 1 <= Nk <= 2^30;
  *          B*H <= 65535. Q, K, V, O 16-byte aligned, LSE 4-byte aligned.
+ * One query per head runs on CUDA cores (bandwidth-bound); 2..16 queries
+ * run both products on the tensor cores with the queries padded to 16.
  * Errors: FA_ERR_INVALID_ARG (pointers, sizes, scale, small workspace),
- * FA_ERR_UNSUPPORTED (FA_F32, d, Nq > 8), FA_ERR_CUDA.
+ * FA_ERR_UNSUPPORTED (FA_F32, d, Nq > 16), FA_ERR_CUDA.
  */
 fa_status fa_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
                     void* workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk, int d,

@@ -101,15 +101,15 @@ def test_decode_rejects_bad_arguments_before_launch(lib):
     assert call(nk=0) == fa.FA_ERR_INVALID_ARG
     assert call(nq=0) == fa.FA_ERR_INVALID_ARG
     assert call(scale=-1.0) == fa.FA_ERR_INVALID_ARG
-    assert call(nq=9) == fa.FA_ERR_UNSUPPORTED
+    assert call(nq=17) == fa.FA_ERR_UNSUPPORTED
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
     assert call(dt=fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
     assert call(B=300, H=300) == fa.FA_ERR_UNSUPPORTED
-    assert lib.fa_decode_workspace_bytes(1, 1, 9, 100, 128, fa.FA_BF16) == 0
+    assert lib.fa_decode_workspace_bytes(1, 1, 17, 100, 128, fa.FA_BF16) == 0
 
 
-def _plan_cost(BH, nk, slots, s):
-    kps = (-(-nk // s) + 63) // 64 * 64
+def _plan_cost(BH, nk, slots, s, tile):
+    kps = (-(-nk // s) + tile - 1) // tile * tile
     return -(-BH * s // slots) * (kps + 128), kps
 
 
@@ -117,11 +117,13 @@ def _plan_cost(BH, nk, slots, s):
     (8, 32, 1, 32768, 304), (1, 1, 1, 1, 304), (1, 1, 4, 1000, 304), (2, 3, 8, 70000, 456),
     (64, 32, 1, 4096, 304), (1, 8, 2, 131072, 608), (4, 4, 1, 100, 3)])
 def test_decode_plan_on_the_host(lib, B, H, nq, nk, slots):
-    """The split plan covers every key with non-empty whole-tile ranges and
+    """The split plan covers every key with non-empty whole-tile ranges (64-key
+    tiles for one query per head, 128-key tensor-core tiles for more) and
     minimises waves x (keys per split + 128) over all admissible split counts."""
+    tile = 64 if nq == 1 else 128
     s, kps = fa.fa_decode_plan(B, H, nq, nk, 128, resident_ctas=slots)
-    assert kps % 64 == 0 and 1 <= s <= 256
+    assert kps % tile == 0 and 1 <= s <= 256
     assert s * kps >= nk and (s - 1) * kps < nk  # covers all keys, no empty range
-    best = min(_plan_cost(B * H, nk, slots, t)[0] for t in range(1, min(256, -(-nk // 64)) + 1)
-               if -(-nk // _plan_cost(B * H, nk, slots, t)[1]) == t)
-    assert _plan_cost(B * H, nk, slots, s)[0] == best
+    best = min(_plan_cost(B * H, nk, slots, t, tile)[0] for t in range(1, min(256, -(-nk // tile)) + 1)
+               if -(-nk // _plan_cost(B * H, nk, slots, t, tile)[1]) == t)
+    assert _plan_cost(B * H, nk, slots, s, tile)[0] == best

@@ -1,6 +1,7 @@
 """GPU parity of KV-cache decode (fa_decode) against the fp64 oracle.
 
-Decode is attention of Nq <= 8 new queries per head against Nk cached keys;
+Decode is attention of Nq <= 16 new queries per head against Nk cached keys
+(one query on CUDA cores, more on the tensor cores);
 the oracle is the plain definition (``attention_fwd`` on the rectangular
 problem). The library splits the keys into ranges and merges the partial
 results; the tests cover one range and many, a ragged last range, fewer keys
@@ -40,14 +41,14 @@ def _run(B, H, nq, nk, d, seed, big_key_every=0):
 
 
 @pytest.mark.parametrize("nk", [1, 17, 63, 64, 65, 1000, 4097])
-@pytest.mark.parametrize("nq", [1, 3, 8])
+@pytest.mark.parametrize("nq", [1, 3, 8, 16])
 @pytest.mark.parametrize("d", [64, 128])
 def test_ragged_cache_lengths(nk, nq, d):
     q, k, v, o, lse, scale = _run(1, 3, nq, nk, d, seed=nk * 10 + nq + d)
     _check(q, k, v, o, lse, scale, [(0, 0), (0, 1), (0, 2)])
 
 
-@pytest.mark.parametrize("nq", [1, 2, 4, 5, 8])
+@pytest.mark.parametrize("nq", [1, 2, 4, 5, 8, 11, 16])
 def test_every_query_bucket_with_many_splits(nq):
     B, H, nk, d = 2, 2, 3000, 128
     splits, kps = fa.fa_decode_plan(B, H, nq, nk, d)
