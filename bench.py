@@ -233,6 +233,25 @@ def blas_threads():
     return os.cpu_count()
 
 
+def cpu_baseline_causal(seconds: float):
+    """The oracle, causal, on whole seeded heads of the workload's shape (the
+    causal mask needs every row's index, so no strips); FLOPs counted as half
+    of the full count, like the GPU line."""
+    from oracle import attention_bwd, attention_fwd
+    flops, heads = 0.0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or heads == 0:
+        q64, k64, v64, do64, scale = oracle_sample_inputs(seed=heads)
+        attention_fwd(q64, k64, v64, scale, causal=True)
+        attention_bwd(q64, k64, v64, do64, scale, causal=True)
+        flops += 0.5 * N * N * D * (4.0 + 10.0)
+        heads += 1
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, causal fwd+bwd of {heads} seeded head(s) of N={N}, d={D}, "
+                      f"{dt:.1f} s (input generation included)"}
+
+
 def cpu_baseline(seconds: float):
     """Time the oracle on the host cores for about `seconds`: fwd+bwd of
     256-row query strips of successive seeded heads of the workload's shape."""
@@ -499,8 +518,8 @@ def run_gpu(args):
     }
     if causal:
         line["config"]["flop_count"] = "causal: half of 4*B*H*N^2*d forward, 2.5x that backward"
-    if world == 1 and not args.no_cpu_baseline and not causal:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = (cpu_baseline_causal if causal else cpu_baseline)(args.cpu_seconds)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -551,8 +570,55 @@ def run_softmax(args):
                      "algorithmic_bytes_per_launch": nbytes},
         "gpu_launches": args.steps,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_softmax(args.cpu_seconds, cols, args.dtype)
     print(json.dumps(line), flush=True)
     return 0
+
+
+def cpu_baseline_softmax(seconds: float, cols: int, dtype: str):
+    """The oracle's row softmax (fp64) on seeded blocks of 256 rows of the same
+    width; bytes counted as the GPU line counts them (each row read and written
+    once in the line's dtype)."""
+    import numpy as np
+    import torch
+
+    from oracle import row_softmax
+    es = 2 if dtype == "bf16" else 4
+    rows_done, blk = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or blk == 0:
+        g = torch.Generator().manual_seed(blk)
+        x = (torch.randn(256, cols, generator=g, dtype=torch.float32) * 4)
+        row_softmax(x.to(torch.float64).numpy())
+        rows_done += 256
+        blk += 1
+    dt = time.perf_counter() - t0
+    return {"value": rows_done * cols * 2 * es / dt / 1e9, "unit": "GB/s", "cores": blas_threads(),
+            "kind": "oracle", "sample": f"fp64 numpy oracle row softmax of {rows_done} rows x {cols} "
+                                        f"columns, {dt:.1f} s (input generation included)"}
+
+
+def cpu_baseline_decode(seconds: float, w):
+    """The oracle (the plain definition over all cached keys) on seeded single
+    heads of the decode workload's shape; bytes counted like the GPU line (K
+    and V of each head once)."""
+    import torch
+
+    from exact_attention_30_gb300.inputs import random_qkv
+    from oracle import attention_fwd
+    heads = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or heads == 0:
+        q, k, v, _ = random_qkv(1, 1, w.Nq, w.d, torch.bfloat16, seed=heads, with_do=False,
+                                big_key_every=64, n_k=w.Nk)
+        f = lambda t: t[0, 0].to(torch.float64).numpy()
+        attention_fwd(f(q), f(k), f(v), w.scale)
+        heads += 1
+    dt = time.perf_counter() - t0
+    return {"value": heads * 4.0 * w.Nk * w.d / dt / 1e9, "unit": "GB/s", "cores": blas_threads(),
+            "kind": "oracle", "sample": f"fp64 numpy oracle decode of {heads} seeded head(s) "
+                                        f"(Nq={w.Nq}, Nk={w.Nk}, d={w.d}), {dt:.1f} s (input generation included)"}
 
 
 def run_decode(args):
@@ -608,6 +674,8 @@ def run_decode(args):
                      "algorithmic_bytes_per_launch": nbytes},
         "gpu_launches": 2 * args.steps,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds, w)
     print(json.dumps(line), flush=True)
     return 0
 
