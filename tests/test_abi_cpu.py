@@ -127,3 +127,37 @@ def test_decode_plan_on_the_host(lib, B, H, nq, nk, slots):
     best = min(_plan_cost(B * H, nk, slots, t, tile)[0] for t in range(1, min(256, -(-nk // tile)) + 1)
                if -(-nk // _plan_cost(B * H, nk, slots, t, tile)[1]) == t)
     assert _plan_cost(B * H, nk, slots, s, tile)[0] == best
+
+
+def test_ex_and_varlen_entry_points_reject_bad_arguments_before_launch(lib):
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    # unknown flags
+    assert lib.fa_fwd_ex(*ok, 1, 2, 64, 64, 0.125, 4, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    ws = fa.fa_bwd_workspace_bytes(1, 2, 64, 64)
+    assert lib.fa_bwd_ex(*([FAKE] * 10), ws, 1, 2, 64, 64, 0.125, 1 << 12, fa.FA_BF16,
+                         None) == fa.FA_ERR_INVALID_ARG
+
+    def fwd_v(cu=FAKE, B=2, H=3, total=100, maxlen=60, d=64, scale=0.125, flags=0, dt=fa.FA_BF16):
+        return lib.fa_fwd_varlen(*ok, cu, B, H, total, maxlen, d, scale, flags, dt, None)
+    assert fwd_v(cu=0) == fa.FA_ERR_INVALID_ARG           # no offsets
+    assert fwd_v(cu=FAKE + 2) == fa.FA_ERR_INVALID_ARG    # misaligned offsets
+    assert fwd_v(maxlen=101) == fa.FA_ERR_INVALID_ARG     # longer than the batch
+    assert fwd_v(total=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd_v(flags=2) == fa.FA_ERR_INVALID_ARG
+    assert fwd_v(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fwd_v(B=70000) == fa.FA_ERR_UNSUPPORTED
+    # workspace sizes: host only, grow with the packed rows, 0 on bad sizes
+    n1 = fa.fa_bwd_varlen_workspace_bytes(2, 3, 100, 60, 64)
+    n2 = fa.fa_bwd_varlen_workspace_bytes(2, 3, 1000, 600, 64)
+    assert 0 < n1 < n2 and n1 % 256 == 0
+    assert lib.fa_bwd_varlen_workspace_bytes(2, 3, 100, 101, 64, fa.FA_BF16) == 0
+    assert lib.fa_bwd_varlen(*([FAKE] * 11), n1 - 1, 2, 3, 100, 60, 64, 0.125, 0, fa.FA_BF16,
+                             None) == fa.FA_ERR_INVALID_ARG  # workspace too small
+
+
+def test_python_binding_checks_varlen_arguments():
+    import torch
+    q = torch.zeros(10, 2, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 10], dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        fa.fa_fwd_varlen(q, q, q, cu, 10)
