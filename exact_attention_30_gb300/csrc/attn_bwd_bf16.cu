@@ -212,10 +212,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
-  // causal grids list bh fastest and the key tiles in increasing order (the
-  // first key tiles see the most query tiles)
-  const int bh = causal ? (int)blockIdx.x : (int)blockIdx.y;
+  // causal grids: (heads of a group, key tiles in increasing order = most
+  // query tiles first, head groups)
+  const int bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
   const int kb = causal ? (int)blockIdx.y : (int)blockIdx.x;
+  if (bh >= a.BH) return;  // past the last head of the last group
   const SeqView sv = seq_view(a.seq, bh, a.status);
   const int N = sv.len;  // queries = keys of this sequence
   const int k0 = kb * C::BK;
@@ -687,7 +688,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
                              C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const unsigned kblocks = (unsigned)((a.seq.N + C::BK - 1) / C::BK);
-    const dim3 grid = a.seq.causal ? dim3((unsigned)BH, kblocks) : dim3(kblocks, (unsigned)BH);
+    dim3 grid(kblocks, (unsigned)BH);
+    if (a.seq.causal) {
+      // every CTA of a head streams the head's Q and dO and adds into its dQ accumulator
+      const int hpg = causal_heads_per_group(BH, 8ll * a.seq.N * D, 48ll << 20);
+      grid = dim3((unsigned)hpg, kblocks, (unsigned)((BH + hpg - 1) / hpg));
+    }
     bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -98,10 +98,11 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
-  // causal grids list bh fastest and the query blocks from the last (most key
-  // tiles) to the first
-  const int bh = causal ? (int)blockIdx.x : (int)blockIdx.y;
+  // causal grids: (heads of a group, query blocks from the last = most key
+  // tiles to the first, head groups)
+  const int bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
   const int qblk = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.x;
+  if (bh >= a.BH) return;  // past the last head of the last group
   const SeqView sv = seq_view(a.seq, bh, a.status);
   const int N = sv.len;  // queries = keys of this sequence
   const int q0 = qblk * (C::BM * C::QT);
@@ -422,7 +423,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, int BH, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const unsigned qblocks = (unsigned)((a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT));
-  const dim3 grid = a.seq.causal ? dim3((unsigned)BH, qblocks) : dim3(qblocks, (unsigned)BH);
+  dim3 grid(qblocks, (unsigned)BH);
+  if (a.seq.causal) {
+    // every CTA of a head streams the head's K and V (budget: most of L2)
+    const int hpg = causal_heads_per_group(BH, 4ll * a.seq.N * D, 96ll << 20);
+    grid = dim3((unsigned)hpg, qblocks, (unsigned)((BH + hpg - 1) / hpg));
+  }
   fwd_bf16_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
   return cudaGetLastError();
 }

@@ -237,6 +237,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.O = O;
   a.LSE = LSE;
   a.seq = sq;
+  a.BH = BH;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.wait_limit_ns = kDefaultWaitLimitNs;
@@ -293,6 +294,7 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.Drow = reinterpret_cast<float*>(ws + L.drow);
   a.seq = sq;
   a.planes = L.planes;
+  a.BH = BH;
   a.ws_rows = L.ws_rows;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;

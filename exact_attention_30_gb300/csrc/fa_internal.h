@@ -54,6 +54,7 @@ struct FwdArgs {
   void* O;      // bf16, SeqArgs layout
   float* LSE;   // SeqArgs statistics layout
   SeqArgs seq;
+  int BH;       // batch * heads
   float scale_log2;  // scale * log2(e)
   int* status;
   unsigned long long wait_limit_ns;
@@ -74,6 +75,7 @@ struct BwdArgs {
   float* Drow;       // fp32 [planes, ws_rows]  -rowsum(dO o O); 0 past the rows
   SeqArgs seq;
   int planes;        // B*H (fixed) or H (variable length)
+  int BH;            // batch * heads
   int ws_rows;       // workspace rows per plane, a multiple of 128: roundup(N, 128)
                      // (fixed length) or roundup(total, 128) + 128 (variable length)
   float scale;
@@ -123,6 +125,19 @@ DecodePlan plan_decode_for_slots(int BH, int Nk, int slots, int tile);
 // cores for one query, 128 on tensor cores for more).
 int decode_tile_keys(int Nq);
 cudaError_t launch_decode_bf16(const DecodeArgs& a, int d, cudaStream_t st);
+
+// Causal grids: (heads of a group, blocks, groups). Within a group of heads
+// the CTAs run longest first; groups run one after the other, each small
+// enough that what its heads' CTAs all stream stays in L2 (bytes_per_head;
+// the backward: Q, dO and the dQ accumulator). Groups are of equal size, so
+// that the last one is not a short tail of heavy CTAs.
+inline int causal_heads_per_group(int BH, long long bytes_per_head, long long budget) {
+  long long g = bytes_per_head > 0 ? budget / bytes_per_head : BH;
+  if (g < 1) g = 1;
+  if (g >= BH) return BH;
+  const long long groups = (BH + g - 1) / g;
+  return (int)((BH + groups - 1) / groups);
+}
 
 // Bounded-wait probe (fa_debug_timeout_probe).
 cudaError_t launch_timeout_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
