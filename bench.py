@@ -63,6 +63,9 @@ def parse_args():
                    default=None, help="another decode shape (profiling captures); the JSON line names it")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "f32"],
                    help="element type for --op softmax")
+    p.add_argument("--varlen", action="store_true",
+                   help="packed variable-length batch: 16 sequences of seeded lengths in [512, 8192], "
+                        "H=16, d=128, fwd+bwd (with --causal: causal); not the headline line")
     p.add_argument("--causal", action="store_true",
                    help="causal attention (FLOPs counted as half of the full count, the usual "
                         "convention; the JSON line names it)")
@@ -680,10 +683,89 @@ def run_decode(args):
     return 0
 
 
+def varlen_lengths(n=16, lo=512, hi=8192, seed=0):
+    """Seeded sequence lengths of the variable-length workload."""
+    import numpy as np
+    return [int(x) for x in np.random.default_rng(seed).integers(lo, hi + 1, size=n)]
+
+
+def run_varlen(args):
+    """fa_fwd_varlen + fa_bwd_varlen on a packed batch of mixed lengths."""
+    import torch
+
+    import exact_attention_30_gb300 as fa
+    from exact_attention_30_gb300.inputs import random_varlen
+
+    lens = varlen_lengths()
+    Hh, Dd = 16, 128
+    causal = bool(args.causal)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    q, k, v, do, cu = (t.to(dev) for t in random_varlen(lens, Hh, Dd, torch.bfloat16, seed=0))
+    maxlen = max(lens)
+    scale = 1 / math.sqrt(Dd)
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(fa.fa_bwd_varlen_workspace_bytes(len(lens), Hh, q.shape[0], maxlen, Dd),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        o, lse = fa.fa_fwd_varlen(q, k, v, cu, maxlen, scale, causal=causal)
+        if ev is not None:
+            ev[1].record(stream)
+        fa.fa_bwd_varlen(q, k, v, o, do, lse, cu, maxlen, scale, causal=causal, workspace=ws)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for e in ev:
+        flush.zero_()
+        step(e)
+    torch.cuda.synchronize(dev)
+    if fa.fa_check_device_status(dev) != fa.FA_OK:
+        raise RuntimeError("device status not OK")
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / len(ev)
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / len(ev)
+    f = 0.5 if causal else 1.0
+    fwd_flops = sum(4.0 * Hh * n * n * Dd for n in lens) * f
+    step_flops = fwd_flops * 3.5
+    value = step_flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+    peaks, src = read_peaks()
+    line = {
+        "metric": "variable-length attention fwd/bwd TFLOP/s (bf16)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": fwd_ms + bwd_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"packed batch of {len(lens)} sequences, lengths {lens} (seeded), "
+                               f"H={Hh}, d={Dd}, {'causal' if causal else 'non-causal'}",
+                   "total_rows": int(q.shape[0]), "flops_per_step": step_flops,
+                   "flop_count": "sum over sequences of 4*H*n^2*d forward (half if causal), 2.5x backward",
+                   "l2": "flushed before every step"},
+        "components": {"fwd": {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12},
+                       "bwd": {"ms": bwd_ms, "tflops": 2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12}},
+        "roofline": {"kernel": "fwd_bf16_kernel + bwd stages (one step)", "bound": "tensor",
+                     "achieved": value, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": value / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": f"{src} bf16 burst"},
+        "gpu_launches": 4 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.op == "softmax":
         return run_softmax(args)
+    if args.varlen:
+        return run_varlen(args)
     if args.op == "decode":
         return run_decode(args)
     if args.impl == "reference":
