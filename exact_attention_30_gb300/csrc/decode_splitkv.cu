@@ -388,8 +388,9 @@ struct DecTcCfg {
   static constexpr int BK = 128;   // keys per tile
   static constexpr int NQP = 16;   // queries padded to the MMA's N
   // d = 128: one CTA per SM, three 64 KB K+V stages keep two tiles loading
-  // while one is processed; d = 64: two CTAs per SM with three 32 KB stages
-  static constexpr int STAGES = 3;
+  // while one is processed; d = 64: three CTAs per SM (96 registers each)
+  // with two 32 KB stages each
+  static constexpr int STAGES = D == 128 ? 3 : 2;
   static constexpr int CH = D / 64;
   static constexpr int CHUNK = BK * 128;     // 128 rows x 128 bytes, swizzled
   static constexpr int TILE = CH * CHUNK;    // a K or a V tile
@@ -406,7 +407,9 @@ struct DecTcCfg {
   // p_empty[2], o_done, red, drain
   static constexpr int NBAR = 2 * STAGES + 1 + 8 + 3;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16;
-  static constexpr int SMEM_ALLOC = SMEM + 1024;
+  // d = 64: no alignment slack, so that three CTAs fit on an SM (the kernel
+  // checks that the dynamic shared memory starts on a 1024-byte boundary)
+  static constexpr int SMEM_ALLOC = D == 64 ? SMEM : SMEM + 1024;
   static constexpr int THREADS = 192;
   static constexpr uint32_t TMEM_COLS = 64;  // S^T x 2 (16 columns each), O^T (16)
   static constexpr uint32_t COL_S = 0, COL_O = 32;
@@ -450,11 +453,16 @@ __device__ __forceinline__ int reduce16_query(int lane) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) decode_tc_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(192, D == 64 ? 3 : 1) decode_tc_kernel(const __grid_constant__ DecodeArgs a) {
   using C = DecTcCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t pad = ((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw);
+  if (pad + C::SMEM > (uint32_t)C::SMEM_ALLOC) {
+    // cannot place the swizzled tiles: report and leave before touching anything
+    if (threadIdx.x == 0) report_status(a.status, kStatusTimeout);
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + C::OFF_BAR;
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
