@@ -27,7 +27,8 @@
 // "Lesson 1" §4: every term is normalised to one common max). When m_ref
 // moves, the row of O in TMEM is multiplied by 2^(m_old - m_new) before the
 // next P V product is issued. P is rounded to bf16 and written over the S
-// columns it came from (the A operand of the TS MMA).
+// columns it came from (d = 128), or into columns of its own (d = 64, where
+// TMEM has room); either way it is the A operand of the TS MMA.
 // Epilogue: O / l to bf16, LSE = (m_ref + log2 l) * ln 2, rows >= N skipped.
 //
 // Sequences: a CTA works on one sequence of the SeqArgs layout (fixed length,
@@ -67,15 +68,81 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + QT * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-  static constexpr int NBAR = 1 + 4 * STAGES + 3 * QT + 1;
+  static constexpr int NBAR = 1 + 4 * STAGES + 4 * QT + 1;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  // TMEM columns: S_t at 128*t, O_t at 256 + D*t
+  // TMEM columns: S_t at 128*t, O_t at 256 + D*t. With d = 64 the last 128
+  // columns are free and hold P_t (64 columns of bf16 pairs each), so P can
+  // be written while S is still being read; with d = 128 P goes over S.
+  static constexpr bool P_OWN = (D == 64);
   static constexpr uint32_t S_COL(int t) { return 128u * t; }
   static constexpr uint32_t O_COL(int t) { return 256u + (uint32_t)D * t; }
+  static constexpr uint32_t P_COL(int t) { return P_OWN ? 256u + 2u * D + 64u * t : S_COL(t); }
 };
+
+// Scores past `valid` (ragged tail, causal diagonal) become -inf.
+__device__ __forceinline__ void mask_cols32(uint32_t (&r)[32], int c0, int valid) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = c0 + i >= valid ? __float_as_uint(-INFINITY) : r[i];
+}
+
+// One 32-column chunk of a row of S: p = 2^(s*c2 - m) for column pairs
+// (packed fp32 arithmetic), the row sums in four packed accumulators, the row
+// max alongside when asked, and the chunk's P as bf16 pairs.
+template <bool WITH_MAX>
+__device__ __forceinline__ void softmax_chunk32(const uint32_t (&r)[32], uint32_t (&pk)[16],
+                                                uint64_t c22, uint64_t nm2, float (&mx)[4],
+                                                uint64_t (&sm2)[4]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+    if (WITH_MAX) mx[i & 3] = fmax3(mx[i & 3], s0, s1);
+    const float2 x = f2_unpack(ffma2(f2_pack(s0, s1), c22, nm2));
+    const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+    sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+}
+
+// A 128-column row of S read in four 32-column chunks, each load in flight
+// while the chunk before it is exponentiated; each chunk's P goes to TMEM
+// columns of its own. Before the first P store the thread waits for the
+// previous P V product to finish reading those columns (o_wait, on the
+// o_done barrier); false if that bounded wait expired (nothing stored then).
+template <bool WITH_MAX>
+__device__ __forceinline__ bool softmax_pass_own_p(uint32_t s_addr, uint32_t p_addr,
+                                                   bool mask_tile, int valid, uint64_t c22,
+                                                   uint64_t nm2, float (&mx)[4],
+                                                   uint64_t (&sm2)[4], bool o_wait,
+                                                   uint32_t o_done, uint32_t o_parity,
+                                                   int* status, unsigned long long limit_ns) {
+  uint32_t ra[32], rb[32], pk[16];
+  tmem_ld32(s_addr, ra);
+  tmem_ld_wait_dep(ra);
+  // not unrolled: fully unrolled, ptxas batches the exponentials of all the
+  // chunks and runs out of registers at the 384-thread cap
+#pragma unroll 1
+  for (int c = 0; c < 4; c += 2) {
+    tmem_ld32(s_addr + 32 * (c + 1), rb);
+    if (mask_tile) mask_cols32(ra, 32 * c, valid);
+    softmax_chunk32<WITH_MAX>(ra, pk, c22, nm2, mx, sm2);
+    if (c == 0 && o_wait &&
+        !__all_sync(0xffffffffu, mbar_wait(o_done, o_parity, status, limit_ns))) {
+      tmem_ld_wait();  // the load in flight lands before its registers go away
+      return false;
+    }
+    tmem_st16(p_addr + 16 * c, pk);
+    tmem_ld_wait_dep(rb);
+    if (c + 2 < 4) tmem_ld32(s_addr + 32 * (c + 2), ra);
+    if (mask_tile) mask_cols32(rb, 32 * (c + 1), valid);
+    softmax_chunk32<WITH_MAX>(rb, pk, c22, nm2, mx, sm2);
+    tmem_st16(p_addr + 16 * (c + 1), pk);
+    if (c + 2 < 4) tmem_ld_wait_dep(ra);
+  }
+  return true;
+}
 
 template <int D>
 __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
@@ -92,7 +159,8 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
   const int B_KFULL = 1, B_VFULL = 1 + C::STAGES, B_KEMPTY = 1 + 2 * C::STAGES,
             B_VEMPTY = 1 + 3 * C::STAGES;
   const int B_SFULL = 1 + 4 * C::STAGES, B_PFULL = B_SFULL + C::QT, B_ODONE = B_PFULL + C::QT;
-  const int B_DRAIN = B_ODONE + C::QT;
+  const int B_SFREE = B_ODONE + C::QT;  // S read by the softmax (own-P layout only)
+  const int B_DRAIN = B_SFREE + C::QT;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
 
@@ -128,6 +196,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       mbar_init(BAR(B_SFULL + t), 1);
       mbar_init(BAR(B_PFULL + t), 4);  // one arrival per softmax warp
       mbar_init(BAR(B_ODONE + t), 1);
+      mbar_init(BAR(B_SFREE + t), 4);
     }
     mbar_init(BAR(B_DRAIN), 1);
     *abort_flag = 0;
@@ -207,7 +276,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       };
       auto issue_pv = [&](int t, int s, bool acc) {
         const uint64_t vb = dV0 + (uint64_t)((s * C::TILE_BYTES) >> 4);
-        const uint32_t dcol = tmem + C::O_COL(t), acol = tmem + C::S_COL(t);
+        const uint32_t dcol = tmem + C::O_COL(t), acol = tmem + C::P_COL(t);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
           mma_ts(dcol, acol + kk * 8, vb + (uint64_t)((kk * 2048) >> 4), idesc_o,
@@ -231,21 +300,44 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         const uint32_t ph = (j / C::STAGES) & 1;
         const int s1 = (j + 1) % C::STAGES;
         const uint32_t ph1 = ((j + 1) / C::STAGES) & 1;
-        if (!wait(B_VFULL + s, ph)) { ok = false; break; }
         bool k_next = false;  // K_{j+1} has landed
+        bool v_here = false;  // V_j has landed
         for (int t = 0; t < C::QT; ++t) {
           const int n_own = t == 0 ? n_t0 : n_t1;
           if (j >= n_own) continue;  // this query tile is past its diagonal
-          if (!wait(B_PFULL + t, j & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          mma_commit(BAR(B_ODONE + t), leader);
-          if (j + 1 < n_own) {
-            if (!k_next && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
-            k_next = true;
+          if constexpr (C::P_OWN) {
+            // P has its own columns: S_{j+1} may overwrite S_j as soon as the
+            // softmax has read it, so it goes first and is ready when the
+            // softmax of tile j is done; P_j V_j follows.
+            if (j + 1 < n_own) {
+              if (!wait(B_SFREE + t, j & 1)) { ok = false; break; }
+              if (!k_next && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
+              k_next = true;
+              tc_fence_after();
+              issue_s(t, s1);
+              mma_commit(BAR(B_SFULL + t), leader);
+            }
+            if (!wait(B_PFULL + t, j & 1)) { ok = false; break; }
+            if (!v_here && !wait(B_VFULL + s, ph)) { ok = false; break; }
+            v_here = true;
             tc_fence_after();
-            issue_s(t, s1);
-            mma_commit(BAR(B_SFULL + t), leader);
+            issue_pv(t, s, j > 0);
+            mma_commit(BAR(B_ODONE + t), leader);
+          } else {
+            // P overwrites S: P_j V_j must be issued before S_{j+1}.
+            if (!v_here && !wait(B_VFULL + s, ph)) { ok = false; break; }
+            v_here = true;
+            if (!wait(B_PFULL + t, j & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            mma_commit(BAR(B_ODONE + t), leader);
+            if (j + 1 < n_own) {
+              if (!k_next && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
+              k_next = true;
+              tc_fence_after();
+              issue_s(t, s1);
+              mma_commit(BAR(B_SFULL + t), leader);
+            }
           }
         }
         if (!ok) break;
@@ -275,8 +367,8 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       bool w = mbar_wait(BAR(B_SFULL + t), j & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      // Raw scores of this row, 64 columns at a time (two 32-column loads, one
-      // wait). Only the last key tile of a query tile can hold masked columns:
+      // Raw scores of this row (d = 128: 64 columns at a time, two 32-column
+      // loads, one wait). Only the last key tile of a query tile can hold masked columns:
       // keys past the sequence's end, and (causal) keys after this row.
       uint32_t r[64];
       const bool mask_tile = j == n_own - 1;
@@ -303,59 +395,94 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       // also leaves issue slots to the MMA warp sharing these sub-partitions.
       float mx[4];
       uint64_t sm2[4];
-      uint32_t pk[64];
       const uint64_t c22 = f2_pack(c2, c2);
 #pragma unroll
       for (int u = 0; u < 4; ++u) { mx[u] = -INFINITY; sm2[u] = 0ull; }
-      {
-        const float neg_m = (j > 0) ? -m_ref : 0.f;
-        const uint64_t nm2 = f2_pack(neg_m, neg_m);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          load_half(h);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-            mx[i & 3] = fmax3(mx[i & 3], s0, s1);
-            const float2 x = f2_unpack(ffma2(f2_pack(s0, s1), c22, nm2));
-            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-            sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
-            pk[32 * h + i] = pack_bf16x2(p0, p1);
-          }
-        }
-      }
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
-      const bool need = mt > m_ref + kRescaleLog2;
+      float mt;
+      bool need;
       float alpha = 1.f;
-      if (__any_sync(0xffffffffu, need)) {
-        // redo for the whole warp (rows that keep their max recompute the
-        // same values)
-        const float m_new = need ? mt : m_ref;
-        alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-        const uint64_t nm2 = f2_pack(-m_new, -m_new);
+      if constexpr (C::P_OWN) {
+        // P has columns of its own: S is read in 32-column chunks, the next
+        // chunk's load in flight while the current one is exponentiated, and
+        // each chunk's P goes to TMEM at once (no register copy of the tile).
+        // S_j was issued before P_{j-1} V_{j-1}, which must have finished
+        // reading P's columns before the first store.
+        const uint32_t p_addr = lane_addr + C::P_COL(t);
+        const float neg_m = (j > 0) ? -m_ref : 0.f;
+        if (!softmax_pass_own_p<true>(s_addr, p_addr, mask_tile, valid, c22, f2_pack(neg_m, neg_m),
+                                      mx, sm2, j > 0, BAR(B_ODONE + t), (uint32_t)(j - 1) & 1u,
+                                      a.status, a.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+        need = mt > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mt : m_ref;
+          alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) sm2[u] = 0ull;
+          for (int u = 0; u < 4; ++u) sm2[u] = 0ull;
+          tmem_st_wait();  // the speculative P is overwritten below
+          softmax_pass_own_p<false>(s_addr, p_addr, mask_tile, valid, c22, f2_pack(-m_new, -m_new),
+                                    mx, sm2, false, 0u, 0u, a.status, a.wait_limit_ns);
+          m_ref = m_new;
+        }
+        // S_j has been read: S_{j+1} may be written over it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_SFREE + t));
+      } else {
+        uint32_t pk[64];
+        {
+          const float neg_m = (j > 0) ? -m_ref : 0.f;
+          const uint64_t nm2 = f2_pack(neg_m, neg_m);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          load_half(h);
+          for (int h = 0; h < 2; ++h) {
+            load_half(h);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 x = f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c22, nm2));
-            const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-            sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
-            pk[32 * h + i] = pack_bf16x2(p0, p1);
+            for (int i = 0; i < 32; ++i) {
+              const float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+              mx[i & 3] = fmax3(mx[i & 3], s0, s1);
+              const float2 x = f2_unpack(ffma2(f2_pack(s0, s1), c22, nm2));
+              const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
+              pk[32 * h + i] = pack_bf16x2(p0, p1);
+            }
           }
         }
-        m_ref = m_new;
+        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+        need = mt > m_ref + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          // redo for the whole warp (rows that keep their max recompute the
+          // same values)
+          const float m_new = need ? mt : m_ref;
+          alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+          const uint64_t nm2 = f2_pack(-m_new, -m_new);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) sm2[u] = 0ull;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            load_half(h);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float2 x = f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c22, nm2));
+              const float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+              sm2[i & 3] = fadd2(sm2[i & 3], f2_pack(p0, p1));
+              pk[32 * h + i] = pack_bf16x2(p0, p1);
+            }
+          }
+          m_ref = m_new;
+        }
+        // P (bf16) over the first 64 S columns
+        tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       }
-      // P (bf16) over the first 64 S columns
-      tmem_st32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       const float2 sa = f2_unpack(fadd2(fadd2(sm2[0], sm2[1]), fadd2(sm2[2], sm2[3])));
       l = l * alpha + (sa.x + sa.y);
-      // P V of the previous tile is complete here: S of this tile was
-      // committed after it, and a commit tracks every earlier MMA. So O can be
-      // rescaled without waiting on o_done (only the epilogue waits on it).
+      // P V of the previous tile is complete here: with P over S, S of this
+      // tile was committed after it (a commit tracks every earlier MMA); with
+      // P in its own columns the pass above waited on o_done. So O can be
+      // rescaled at once.
       if (j > 0) {
         if (__any_sync(0xffffffffu, need)) {  // alpha == 1 on rows whose max did not move
 #pragma unroll
