@@ -21,13 +21,13 @@
 //                  dV += P^T dO_i (P^T read from TMEM), dK += dS^T Q_i
 //                  dQ_i^T = K_j^T dS^T (d = 128) or dQ_i = dS K_j (d = 64)
 //                  -> added into the fp32 accumulator (TMA tensor reduce-add
-//                  from shared memory at d = 128, fp32 atomics at d = 64)
+//                  from shared-memory staging blocks)
 //                A softmax warpgroup (one thread per key) first writes bf16
 //                P^T over the S^T columns, then, once dP^T is there, writes
 //                bf16 dS^T into a swizzled shared-memory tile that feeds both
 //                dK (K-major view) and dQ (MN-major view). dQ_i is computed
 //                into the dP^T columns; a dQ warpgroup reads it out and adds
-//                it to the accumulator with 16-byte atomics. Per query tile the
+//                it to the accumulator as above. Per query tile the
 //                MMA order is dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1), so the
 //                next tile's recompute overlaps this tile's softmax.
 //  3. dq_convert: fp32 accumulator times scale -> bf16 dQ.
@@ -134,9 +134,10 @@ template <int D>
 struct BwdCfg {
   static constexpr int BK = 128;  // keys per CTA: TMEM lanes of S^T, dP^T, dV, dK
   static constexpr int BQ = 128;  // queries per streamed tile
-  // d = 128 computes dQ^T = K^T dS^T (d on the TMEM lanes) so that a warp's
-  // fp32 atomics cover one contiguous 128-byte row segment; d = 64 computes
-  // dQ = dS K (queries on the lanes; an M = 64 product would be needed otherwise)
+  // d = 128 computes dQ^T = K^T dS^T (d on the TMEM lanes: a warp's lanes
+  // fill one 128-byte row segment of a staging block); d = 64 computes
+  // dQ = dS K (queries on the lanes; an M = 64 product would be needed
+  // otherwise) and stages each lane's row through a swizzled block
   static constexpr bool DQ_T = (D == 128);
   static constexpr int CH = D / 64;                  // 128-byte chunks per K/V/Q/dO row
   // Q_i (with its LSE/D statistics) is read by S^T(i), issued one tile
@@ -157,13 +158,15 @@ struct BwdCfg {
   static constexpr int OFF_DO = OFF_Q + QSTAGES * TILE;
   static constexpr int OFF_STAT = OFF_DO + DOSTAGES * TILE;
   static constexpr int STATSTAGES = 2;  // LSE*log2e and D, read by both softmax phases
-  // dQ reduction staging (d = 128): per dQ warp 2 x [32 queries][32 d] fp32,
-  // added into the global accumulator by the TMA engine (tensor bulk
-  // reduce-add) instead of fp32 atomics
+  // dQ reduction staging: per dQ warp 2 x [32 queries][32 d] fp32, added
+  // into the global accumulator by the TMA engine (tensor bulk reduce-add)
+  // instead of fp32 atomics. 1024-byte aligned (the d = 64 blocks are
+  // written in the TMA 128-byte swizzle).
   static constexpr int DQ_ROWS = 32;
   static constexpr int DQ_BLOCK_BYTES = DQ_ROWS * 32 * 4;  // 4 KB
   static constexpr int OFF_DQS = OFF_STAT + STATSTAGES * STAT_BYTES;
-  static constexpr int OFF_BAR = OFF_DQS + (DQ_T ? 4 * 2 * DQ_BLOCK_BYTES : 0);
+  static constexpr int OFF_BAR = OFF_DQS + 4 * 2 * DQ_BLOCK_BYTES;
+  static_assert(OFF_DQS % 1024 == 0, "swizzled staging alignment");
   // barriers: kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], st_full[2],
   //           st_empty[2], s_full, dp_full, pt_ready, ds_ready, ds_empty, dq_full,
   //           dq_empty, acc_done, drain
@@ -649,12 +652,28 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             }
           }
         } else {
-          // lane t holds this half of the dQ row of query row0 + t
-          float4* base = reinterpret_cast<float4*>(a.dQacc + (row0 + t) * D + HALF * hh);
+          // lane t holds this half (32 columns) of the dQ row of query
+          // row0 + t. The warp stages its 32 rows x 32 columns as [row][32]
+          // fp32 in the TMA 128-byte swizzle (16-byte unit k of row r at unit
+          // k ^ (r % 8): the float4 stores of the 32 lanes hit every bank
+          // equally) and lets the TMA engine add the block into the
+          // accumulator; two buffers per warp, tracked by the warp's lane 0.
+          const int buf = nblk & 1;
+          if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
+          __syncwarp();
+          uint8_t* stage = wstage + buf * C::DQ_BLOCK_BYTES;
 #pragma unroll
-          for (int q = 0; q < HALF / 4; ++q)
-            atomicAdd(base + q, make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+          for (int k = 0; k < HALF / 4; ++k)
+            *reinterpret_cast<float4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                            __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), HALF * hh, (int)(row0 + (size_t)wq * 32));
+            bulk_commit_group();
+          }
+          ++nblk;
         }
       }
     }

@@ -68,14 +68,18 @@ bool encode_bhnd_bf16(CUtensorMap* m, const void* ptr, int BH, int N, int d, int
   return encode_seq_bf16(m, ptr, sq, BH, d, box_rows);
 }
 
-// fp32 [rows, d] accumulator as 2-D (d, rows); 32 x 32 boxes, no swizzle.
+// fp32 [rows, d] accumulator as 2-D (d, rows); 32 x 32 boxes.
 bool encode_acc_f32(CUtensorMap* m, void* ptr, long long rows, int d) {
   cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)d * 4};
   cuuint32_t box[2] = {32, 32};
   cuuint32_t estr[2] = {1, 1};
+  // d = 128 stages [query][32 d] blocks written one d column per lane (no
+  // swizzle needed); d = 64 stages one query row per lane, in the 128-byte
+  // swizzle that keeps those shared-memory stores free of bank conflicts.
+  const CUtensorMapSwizzle sw = d == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

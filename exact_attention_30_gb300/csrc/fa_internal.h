@@ -63,7 +63,7 @@ cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st);
 
 struct BwdArgs {
   CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D (d, rows, planes) views of the SeqArgs layout
-  CUtensorMap tmDQacc;  // fp32 [planes*ws_rows, d], 32 x 32 boxes, no swizzle (d = 128 only)
+  CUtensorMap tmDQacc;  // fp32 [planes*ws_rows, d], 32 x 32 boxes; 128-byte swizzle at d = 64
   const void* O;     // bf16, SeqArgs layout (as Q, K, V, dO, dQ, dK, dV)
   const void* dO;
   const float* LSE;  // SeqArgs statistics layout
