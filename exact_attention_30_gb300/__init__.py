@@ -47,6 +47,9 @@ _SIGNATURES = {
     "fa_fwd": (_ci, [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_fwd_ex": (_ci, [_vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
     "fa_fwd_varlen": (_ci, [_vp] * 6 + [_ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
+    "fa_fwd_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
+    "fa_fwd_ws": (_ci, [_vp] * 6 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
+    "fa_fwd_plan": (_ci, [_ci] * 7 + [ctypes.POINTER(_ci)] * 3),
     "fa_bwd_ex": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
     "fa_bwd_varlen_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
     "fa_bwd_varlen": (_ci, [_vp] * 11 + [_sz, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
@@ -136,8 +139,32 @@ def _raise(code: int, where: str):
         raise FAError(code, where)
 
 
-def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False):
-    """Forward pass: returns (O [B,H,N,d] like q, LSE [B,H,N] float32)."""
+def fa_fwd_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool = False,
+                           dtype=torch.bfloat16) -> int:
+    """Scratch bytes with which the forward splits its last, partly filled
+    wave of CTAs on the current device (0: nothing to gain)."""
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F32
+    return int(load_library().fa_fwd_workspace_bytes(B, H, N, d, FA_CAUSAL if causal else 0, code))
+
+
+def fa_fwd_plan(B: int, H: int, N: int, d: int, causal: bool = False, dtype=torch.bfloat16,
+                resident_ctas: int = 0):
+    """(n_full, n_tail, splits) of the forward's schedule (fa_fwd_plan in fa.h)."""
+    nf, nt, sp = _ci(), _ci(), _ci()
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F32
+    rc = load_library().fa_fwd_plan(B, H, N, d, FA_CAUSAL if causal else 0, code, resident_ctas,
+                                    ctypes.byref(nf), ctypes.byref(nt), ctypes.byref(sp))
+    _raise(rc, "fa_fwd_plan")
+    return nf.value, nt.value, sp.value
+
+
+def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool = False,
+           workspace=None):
+    """Forward pass: returns (O [B,H,N,d] like q, LSE [B,H,N] float32).
+
+    When the problem gains from splitting the tail of the schedule
+    (fa_fwd_workspace_bytes > 0), the scratch is allocated here unless a
+    uint8 CUDA tensor of at least that size is passed as ``workspace``."""
     lib = load_library()
     _check(q, "q")
     _check(k, "k", q)
@@ -151,10 +178,20 @@ def fa_fwd(q, k, v, scale: float | None = None, out=None, lse=None, causal: bool
     _check(o, "out", q)
     if lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_cuda:
         raise ValueError("lse must be float32 [B,H,N] on the same device")
+    flags = FA_CAUSAL if causal else 0
     with torch.cuda.device(q.device):
-        rc = lib.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                           B, H, N, d, scale, FA_CAUSAL if causal else 0, _dtype_code(q),
-                           _stream_ptr(q.device))
+        ws_bytes = int(lib.fa_fwd_workspace_bytes(B, H, N, d, flags, _dtype_code(q)))
+        if ws_bytes > 0 and workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            if workspace.dtype != torch.uint8 or not workspace.is_cuda or workspace.device != q.device:
+                raise ValueError("workspace must be a uint8 tensor on q's device")
+            rc = lib.fa_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               workspace.data_ptr(), workspace.numel(), B, H, N, d, scale, flags,
+                               _dtype_code(q), _stream_ptr(q.device))
+        else:
+            rc = lib.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               B, H, N, d, scale, flags, _dtype_code(q), _stream_ptr(q.device))
     _raise(rc, "fa_fwd")
     return o, lse
 

@@ -46,6 +46,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "fa_internal.h"
 #include "ptx.cuh"
 #include "seq.cuh"
@@ -54,6 +56,7 @@ namespace fa {
 namespace {
 
 constexpr float kRescaleLog2 = 8.0f;  // tolerated growth of the running max before O is rescaled
+constexpr int kMaxTailSplits = 4;     // key ranges of a split unit (the host plan's bound)
 
 template <int D>
 struct FwdCfg {
@@ -164,22 +167,46 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
 
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
-  // causal grids: (heads of a group, query blocks from the last = most key
-  // tiles to the first, head groups)
-  const int bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
-  const int qblk = causal ? (int)(gridDim.y - 1 - blockIdx.y) : (int)blockIdx.x;
+  int bh, qblk;
+  int tail_unit = -1, part = 0;  // split units: index among them, key part
+  if (causal) {
+    // causal grids: (heads of a group, query blocks from the last = most key
+    // tiles to the first, head groups)
+    bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    qblk = (int)(gridDim.y - 1 - blockIdx.y);
+  } else {
+    // one CTA per unit (head, 256-row block), head-major; the units from
+    // n_full on are split into a.splits key ranges, one CTA each
+    const int qblocks = (a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT);
+    int u = (int)blockIdx.x;
+    if (u >= a.n_full) {
+      const int r = u - a.n_full;
+      tail_unit = r / a.splits;
+      part = r - tail_unit * a.splits;
+      u = a.n_full + tail_unit;
+    }
+    bh = u / qblocks;
+    qblk = u - bh * qblocks;
+  }
   if (bh >= a.BH) return;  // past the last head of the last group
   const SeqView sv = seq_view(a.seq, bh, a.status);
   const int N = sv.len;  // queries = keys of this sequence
   const int q0 = qblk * (C::BM * C::QT);
   if (q0 >= N) return;  // the whole CTA: nothing of this sequence here
   const int n_kv = (N + C::BN - 1) / C::BN;
-  // key tiles per query tile: all of them, or up to the diagonal
+  // key tiles kt0 + j, j < n_t0 (query tile 0) or n_t1 (tile 1): all of
+  // them, up to the diagonal (causal), or this CTA's part of a split unit
+  int kt0 = 0, kt_end = n_kv;
+  if (tail_unit >= 0) {
+    kt0 = (int)((long long)part * n_kv / a.splits);
+    kt_end = (int)((long long)(part + 1) * n_kv / a.splits);
+  }
   const int qt0 = q0 / C::BM;
-  const int n_t0 = causal ? min(qt0 + 1, n_kv) : n_kv;
-  const int n_t1 = causal ? min(qt0 + 2, n_kv) : n_kv;  // >= n_t0
+  const int n_t0 = causal ? min(qt0 + 1, n_kv) : kt_end - kt0;
+  const int n_t1 = causal ? min(qt0 + 2, n_kv) : kt_end - kt0;  // >= n_t0
   const int n_max = n_t1;
   const int y0 = sv.start;  // first row of the sequence in the TMA views
   const int plane = sv.plane;
@@ -230,13 +257,13 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         mbar_arrive_expect_tx(BAR(B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmK,
-                      BAR(B_KFULL + s), c * 64, y0 + j * C::BN, plane);
+                      BAR(B_KFULL + s), c * 64, y0 + (kt0 + j) * C::BN, plane);
         last_k[s] = j;
         if (!mbar_wait(BAR(B_VEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(BAR(B_VFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CH; ++c)
           tma_load_3d(sbase + C::OFF_V + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmV,
-                      BAR(B_VFULL + s), c * 64, y0 + j * C::BN, plane);
+                      BAR(B_VFULL + s), c * 64, y0 + (kt0 + j) * C::BN, plane);
         last_v[s] = j;
       }
       // drain: the last load issued into each slot must have landed before exit
@@ -372,7 +399,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       // keys past the sequence's end, and (causal) keys after this row.
       uint32_t r[64];
       const bool mask_tile = j == n_own - 1;
-      int valid = N - j * C::BN;
+      int valid = N - (kt0 + j) * C::BN;  // >= 128 unless this is the sequence's last tile
       if (causal) valid = min(valid, row - j * C::BN + 1);
       auto load_half = [&](int h) {
         tmem_ld32(s_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
@@ -506,27 +533,104 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       const bool w = mbar_wait(BAR(B_ODONE + t), (n_own - 1) & 1, a.status, a.wait_limit_ns);
       ok = __all_sync(0xffffffffu, w);
     }
-    if (!ok) {
-      *abort_flag = 1;
-    } else {
+    if (!ok) *abort_flag = 1;
+    if (tail_unit >= 0) {
+      // One key part of a split unit: its normalised partial O (fp32) and
+      // base-2 LSE go to the workspace; fwd_tail_merge_kernel, launched after
+      // this kernel, combines the parts. Both tiles' products are complete
+      // past the first barrier, so all of shared memory is free: tile t
+      // stages its rows in [OFF_Q + t * D * 512, ...) as 32-column boxes of
+      // 128 rows in the TMA 128-byte swizzle, and one thread stores them.
+      named_bar_sync<1>(256);
+      const int rows_unit = C::BM * C::QT;
+      const int prow0 = (tail_unit * a.splits + part) * rows_unit + t * C::BM;  // tile's first workspace row
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        uint8_t* stage = smem + C::OFF_Q + t * (D * 512);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + 32 * q, r);
+          tmem_ld_wait();
+          uint8_t* box = stage + q * 16384 + row_in_tile * 128;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(box + ((k ^ (row_in_tile & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * k]) * inv_l, __uint_as_float(r[4 * k + 1]) * inv_l,
+                            __uint_as_float(r[4 * k + 2]) * inv_l, __uint_as_float(r[4 * k + 3]) * inv_l);
+        }
+        a.Lpart[prow0 + row_in_tile] = m_ref + __log2f(l);
+        fence_proxy_async_smem();
+      }
+      if (t == 0) named_bar_sync<2>(128);
+      else named_bar_sync<3>(128);
+      if (ok && warp == 4 + 4 * t && lane == 0) {
+        const uint8_t* stage = smem + C::OFF_Q + t * (D * 512);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) tma_store_2d(&a.tmOpart, smem_u32(stage + q * 16384), q * 32, prow0);
+        bulk_commit_group();
+        bulk_wait_group_all();
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) + seq_row_offset(a.seq, sv, row);
+      // A tile that cannot reach past its sequence's rows in the tensor (fixed
+      // length: rows past N are outside the map and not written) leaves
+      // through the tile's Q slot, which its last S product has finished
+      // reading: bf16 rows in the 128-byte swizzle of the TMA box (16-byte
+      // unit k of row r at k ^ (r % 8), so the 32 lanes' stores spread over
+      // all banks), then tensor stores of 64 columns x 128 rows. The other
+      // tiles (a packed sequence's last, partial tile) store row by row.
+      const bool tma_out = a.seq.cu_seqlens == nullptr || q0 + (t + 1) * C::BM <= N;
+      if (tma_out) {
+        uint8_t* stage = smem + C::OFF_Q + t * C::TILE_BYTES;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t r[32];
-        tmem_ld32(o_addr + 32 * q, r);
-        tmem_ld_wait();
-        if (row < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + 32 * q, r);
+          tmem_ld_wait();
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
+            const int c0 = 32 * q + 8 * v;  // first column of this 16-byte unit
             uint4 u;
             u.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
             u.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
             u.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
             u.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-            dst[v] = u;
+            const int k = (c0 & 63) >> 3;
+            *reinterpret_cast<uint4*>(stage + (c0 >> 6) * C::CHUNK_BYTES + row_in_tile * 128 +
+                                      ((k ^ (row_in_tile & 7)) << 4)) = u;
+          }
+        }
+        fence_proxy_async_smem();
+        if (t == 0) named_bar_sync<2>(128);  // this tile's softmax warps
+        else named_bar_sync<3>(128);
+        if (warp == 4 + 4 * t && lane == 0) {
+#pragma unroll
+          for (int c = 0; c < C::CH; ++c)
+            tma_store_3d(&a.tmO, smem_u32(stage + c * C::CHUNK_BYTES), c * 64, y0 + q0 + t * C::BM, plane);
+          bulk_commit_group();
+          bulk_wait_group_all();  // written, and the slot read, before the CTA exits
+        }
+      } else {
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) + seq_row_offset(a.seq, sv, row);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + 32 * q, r);
+          tmem_ld_wait();
+          if (row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * q);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
+              u.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
+              u.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
+              u.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
+              dst[v] = u;
+            }
           }
         }
       }
@@ -542,25 +646,149 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
   }
 }
 
+// Combines the key parts of the split units ("Lesson 1: FlashAttention core
+// idea" §3: partial softmaxes merge through their maxima and sums): row r
+// gets O = sum_p w_p O_p / sum_p w_p with w_p = 2^(L_p - max L), and LSE =
+// (max L + log2 sum_p w_p) ln 2. Warp-wide rows (lanes along d, coalesced),
+// four rows per warp with every part's loads in flight.
+template <int D>
+__global__ void __launch_bounds__(256) fwd_tail_merge_kernel(const __grid_constant__ FwdArgs a) {
+  constexpr int PER = D / 32;  // floats of a row per lane
+  constexpr int RPW = 4;       // rows per warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows_unit = 256;
+  const int qblocks = (a.seq.N + rows_unit - 1) / rows_unit;
+  const long long r_first = (long long)blockIdx.x * (8 * RPW) + warp * RPW;  // merged row: tail unit * 256 + row
+  float lp[RPW][kMaxTailSplits];
+  float x[RPW][kMaxTailSplits][PER];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const long long mr = r_first + i;
+    const long long tu = mr / rows_unit, ru = mr - tu * rows_unit;
+#pragma unroll
+    for (int p = 0; p < kMaxTailSplits; ++p) {
+      lp[i][p] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) x[i][p][e] = 0.f;
+      if (p < a.splits && tu < a.n_tail) {
+        const size_t pr = (size_t)(tu * a.splits + p) * rows_unit + ru;
+        lp[i][p] = a.Lpart[pr];
+        const float* src = a.Opart + pr * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          x[i][p][0] = v.x; x[i][p][1] = v.y; x[i][p][2] = v.z; x[i][p][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          x[i][p][0] = v.x; x[i][p][1] = v.y;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    const long long mr = r_first + i;
+    const long long tu = mr / rows_unit, ru = mr - tu * rows_unit;
+    if (tu >= a.n_tail) continue;
+    const long long u = a.n_full + tu;
+    const long long bh = u / qblocks;
+    const long long row = (u - bh * qblocks) * rows_unit + ru;
+    if (row >= a.seq.N) continue;
+    float L = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kMaxTailSplits; ++p) L = fmaxf(L, lp[i][p]);
+    float w[kMaxTailSplits], wsum = 0.f;
+#pragma unroll
+    for (int p = 0; p < kMaxTailSplits; ++p) {
+      w[p] = exp2f(lp[i][p] - L);  // 0 for the parts past a.splits
+      wsum += w[p];
+    }
+    const float inv_w = 1.f / wsum;
+    float y[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      float acc = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMaxTailSplits; ++p) acc = fmaf(w[p], x[i][p][e], acc);
+      y[e] = acc * inv_w;
+    }
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) + (size_t)bh * (size_t)a.seq.plane_stride +
+                          (size_t)row * (size_t)a.seq.row_stride + lane * PER;
+    if constexpr (PER == 4)
+      *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+    else
+      *reinterpret_cast<uint32_t*>(orow) = pack_bf16x2(y[0], y[1]);
+    if (lane == 0) a.LSE[(size_t)bh * (size_t)a.seq.stat_plane + row] = (L + __log2f(wsum)) * 0.69314718055994531f;
+  }
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdArgs& a, int BH, cudaStream_t st) {
   using C = FwdCfg<D>;
   static_assert(C::SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+  static_assert(C::QT * D * 512 <= C::OFF_BAR - C::OFF_Q, "split-part staging fits the tile buffers");
   cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const unsigned qblocks = (unsigned)((a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT));
-  dim3 grid(qblocks, (unsigned)BH);
+  if (a.splits < 1 || a.splits > kMaxTailSplits || a.n_full < 0 || a.n_tail < 0 ||
+      (a.splits == 1) != (a.n_tail == 0) ||
+      (long long)a.n_full + a.n_tail != (long long)qblocks * BH ||
+      (a.splits > 1 && (a.seq.causal || a.seq.cu_seqlens || a.Opart == nullptr || a.Lpart == nullptr)))
+    return cudaErrorInvalidValue;
+  dim3 grid((unsigned)((long long)a.n_full + (long long)a.n_tail * a.splits));
   if (a.seq.causal) {
     // every CTA of a head streams the head's K and V (budget: most of L2)
     const int hpg = causal_heads_per_group(BH, 4ll * a.seq.N * D, 96ll << 20);
     grid = dim3((unsigned)hpg, qblocks, (unsigned)((BH + hpg - 1) / hpg));
   }
   fwd_bf16_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
+  cudaError_t e2 = cudaGetLastError();
+  if (e2 != cudaSuccess || a.splits == 1) return e2;
+  const long long merge_rows = (long long)a.n_tail * C::BM * C::QT;
+  fwd_tail_merge_kernel<D><<<(unsigned)((merge_rows + 31) / 32), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
+std::mutex g_slots_mu;
+int g_slots[16] = {};
+
 }  // namespace
+
+FwdTailPlan plan_fwd_tail(long long units, int n_kv, int slots) {
+  FwdTailPlan p{(int)units, 0, 1};
+  if (units < 1 || slots < 1 || n_kv < 1) return p;
+  const long long rem = units % slots;
+  if (units < slots || rem == 0) return p;  // no whole wave before the tail, or no tail
+  // Split the tail's units into as many key ranges as fit into one wave, at
+  // most four and with at least four key tiles per range.
+  long long sp = slots / rem;
+  if (sp > 4) sp = 4;
+  if (sp > n_kv / 4) sp = n_kv / 4;
+  if (sp < 2) return p;
+  p.n_full = (int)(units - rem);
+  p.n_tail = (int)rem;
+  p.splits = (int)sp;
+  return p;
+}
+
+size_t fwd_tail_workspace_bytes(const FwdTailPlan& p, int d) {
+  if (p.splits <= 1 || p.n_tail <= 0) return 0;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const size_t rows = (size_t)p.n_tail * p.splits * 256;
+  return up(rows * d * 4) + up(rows * 4);
+}
+
+int fwd_slots() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return 0;
+  std::lock_guard<std::mutex> lk(g_slots_mu);
+  if (g_slots[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_slots[dev] = sms;  // one forward CTA per SM (all of TMEM, most of shared memory)
+  }
+  return g_slots[dev];
+}
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st) {
   if (d == 128) return launch_fwd_d<128>(a, BH, st);

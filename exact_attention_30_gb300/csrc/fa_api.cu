@@ -84,6 +84,19 @@ bool encode_acc_f32(CUtensorMap* m, void* ptr, long long rows, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// Partial O of the forward's split units: fp32 [rows, d] as 2-D (d, rows),
+// boxes of 32 columns (128 bytes) x 128 rows in the 128-byte swizzle.
+bool encode_part_f32(CUtensorMap* m, void* ptr, long long rows, int d) {
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_dtype_d(int d, fa_dtype dt) {
@@ -214,8 +227,18 @@ using namespace fa;
 
 namespace {
 
+// Tail split of the bf16 forward for this problem on the current device (only
+// fixed-length, non-causal problems are split; the others: one plain plan).
+FwdTailPlan fwd_tail_plan(const SeqArgs& sq, int BH, fa_dtype dt) {
+  const long long qblocks = ((long long)sq.N + 255) / 256;
+  const long long units = qblocks * BH;
+  if (dt != FA_BF16 || sq.causal || sq.cu_seqlens) return FwdTailPlan{(int)units, 0, 1};
+  return plan_fwd_tail(units, (sq.N + 127) / 128, fwd_slots());
+}
+
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                   const SeqArgs& sq, int B, int d, float scale, fa_dtype dt, void* stream) {
+                   const SeqArgs& sq, int B, int d, float scale, fa_dtype dt, void* stream,
+                   void* workspace = nullptr, size_t workspace_bytes = 0) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   const size_t al = dt == FA_BF16 ? 16 : 4;
   if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) || !aligned(LSE, 4))
@@ -236,7 +259,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   if (!encode_seq_bf16(&a.tmQ, Q, sq, planes, d, 128) || !encode_seq_bf16(&a.tmK, K, sq, planes, d, 128) ||
-      !encode_seq_bf16(&a.tmV, V, sq, planes, d, 128))
+      !encode_seq_bf16(&a.tmV, V, sq, planes, d, 128) || !encode_seq_bf16(&a.tmO, O, sq, planes, d, 128))
     return FA_ERR_CUDA;
   a.O = O;
   a.LSE = LSE;
@@ -245,6 +268,22 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.wait_limit_ns = kDefaultWaitLimitNs;
+  FwdTailPlan plan = fwd_tail_plan(sq, BH, dt);
+  const size_t need = fwd_tail_workspace_bytes(plan, d);
+  if (workspace != nullptr && need > 0) {
+    if (!aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    const size_t rows = (size_t)plan.n_tail * plan.splits * 256;
+    const size_t o_bytes = (rows * d * 4 + 255) & ~(size_t)255;
+    char* ws = static_cast<char*>(workspace);
+    a.Opart = reinterpret_cast<float*>(ws);
+    a.Lpart = reinterpret_cast<float*>(ws + o_bytes);
+    if (!encode_part_f32(&a.tmOpart, a.Opart, (long long)rows, d)) return FA_ERR_CUDA;
+  } else {
+    plan = FwdTailPlan{plan.n_full + plan.n_tail, 0, 1};  // no scratch: every unit runs whole
+  }
+  a.n_full = plan.n_full;
+  a.n_tail = plan.n_tail;
+  a.splits = plan.splits;
   return launch_fwd_bf16(a, BH, d, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -335,6 +374,41 @@ fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float*
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
                  int N, int d, float scale, fa_dtype dt, void* stream) {
   return fa_fwd_ex(Q, K, V, O, LSE, B, H, N, d, scale, 0, dt, stream);
+}
+
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int flags, fa_dtype dt) {
+  if (check_shape(B, H, N, d, 1.f, dt) != FA_OK || (flags & ~FA_CAUSAL)) return 0;
+  const SeqArgs sq = fixed_seq(H, N, d, flags & FA_CAUSAL);
+  return fwd_tail_workspace_bytes(fwd_tail_plan(sq, B * H, dt), d);
+}
+
+fa_status fa_fwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int resident_ctas,
+                      int* n_full, int* n_tail, int* splits) {
+  if (!n_full || !n_tail || !splits || resident_ctas < 0) return FA_ERR_INVALID_ARG;
+  const fa_status s = check_shape(B, H, N, d, 1.f, dt);
+  if (s != FA_OK) return s;
+  if (flags & ~FA_CAUSAL) return FA_ERR_INVALID_ARG;
+  const SeqArgs sq = fixed_seq(H, N, d, flags & FA_CAUSAL);
+  const long long units = ((long long)N + 255) / 256 * B * H;
+  FwdTailPlan p{(int)units, 0, 1};
+  if (resident_ctas == 0)
+    p = fwd_tail_plan(sq, B * H, dt);
+  else if (dt == FA_BF16 && !(flags & FA_CAUSAL))
+    p = plan_fwd_tail(units, (N + 127) / 128, resident_ctas);
+  *n_full = p.n_full;
+  *n_tail = p.n_tail;
+  *splits = p.splits;
+  return FA_OK;
+}
+
+fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                    float scale, int flags, fa_dtype dt, void* stream) {
+  const fa_status s = check_shape(B, H, N, d, scale, dt);
+  if (s != FA_OK) return s;
+  if (flags & ~FA_CAUSAL) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, fixed_seq(H, N, d, flags & FA_CAUSAL), B, d, scale, dt, stream,
+                  workspace, workspace_bytes);
 }
 
 fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,

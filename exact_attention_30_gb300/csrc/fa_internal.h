@@ -51,6 +51,7 @@ cudaError_t launch_bwd_f32(const float* Q, const float* K, const float* V, const
 // planes) with 64-element x {128, 64}-row boxes and 128-byte swizzle.
 struct FwdArgs {
   CUtensorMap tmQ, tmK, tmV;  // 3-D (d, rows, planes) views of the SeqArgs layout
+  CUtensorMap tmO;            // the same view of O (epilogue tensor stores)
   void* O;      // bf16, SeqArgs layout
   float* LSE;   // SeqArgs statistics layout
   SeqArgs seq;
@@ -58,8 +59,29 @@ struct FwdArgs {
   float scale_log2;  // scale * log2(e)
   int* status;
   unsigned long long wait_limit_ns;
+  // Tail split (fixed length, non-causal): units (head, 256-row block)
+  // 0..n_full-1 run whole; the n_tail units after them run as `splits` key
+  // ranges each, and a second kernel merges the partial results. splits = 1
+  // and n_full = every unit when nothing is split.
+  int n_full, n_tail, splits;
+  float* Opart;        // fp32 [n_tail][splits][256][d]: normalised partial O
+  float* Lpart;        // fp32 [n_tail][splits][256]: base-2 log-sum-exp of each part
+  CUtensorMap tmOpart;  // Opart as 2-D (d, rows), 32 x 128 boxes, 128-byte swizzle
 };
 cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st);
+
+// The tail split of the bf16 forward for `units` units of n_kv key tiles on
+// a GPU that runs `slots` forward CTAs at once: the units of the last,
+// partly filled wave are split when that shortens the makespan (whole waves
+// + 1/splits instead of + 1).
+struct FwdTailPlan {
+  int n_full, n_tail, splits;
+};
+FwdTailPlan plan_fwd_tail(long long units, int n_kv, int slots);
+// Scratch for a plan: partial O, partial LSE (256-byte aligned parts).
+size_t fwd_tail_workspace_bytes(const FwdTailPlan& p, int d);
+// Forward CTAs resident at once on the current device (one per SM).
+int fwd_slots();
 
 struct BwdArgs {
   CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D (d, rows, planes) views of the SeqArgs layout

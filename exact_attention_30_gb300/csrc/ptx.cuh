@@ -85,6 +85,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
 
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (TMA / tensor core operand reads).
+// Barrier ID (1..15) among `count` threads of the block (a multiple of 32).
+template <int ID>
+__device__ __forceinline__ void named_bar_sync(int count) {
+  static_assert(ID >= 1 && ID <= 15, "named barrier id");
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -125,6 +131,24 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
       "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
       "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+// Tensor store of a shared-memory box to global memory (2-D map), tracked by
+// this thread's bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(src)
+      : "memory");
+}
+// Tensor store of a shared-memory box to global memory (3-D map), tracked by
+// this thread's bulk groups. Out-of-range rows of the box are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {

@@ -86,6 +86,45 @@ fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float*
                     int B, int H, int N, int d, float scale, int flags, fa_dtype dt, void* stream);
 
 /*
+ * Bytes of device scratch with which fa_fwd_ws shortens this problem's
+ * forward on the CURRENT device; 0 when it gains nothing (or on invalid
+ * arguments). Only bf16, non-causal problems are split.
+ */
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int flags, fa_dtype dt);
+
+/*
+ * The schedule fa_fwd_ws uses: *n_full units (batch*head, 256-query block)
+ * run whole, then *n_tail units run as *splits key ranges each (*splits = 1,
+ * *n_tail = 0: nothing split). resident_ctas > 0 plans for a GPU running
+ * that many forward CTAs at once (host only, no GPU needed); 0 plans for the
+ * current device. The rule: with W CTAs at once and U units, the U mod W
+ * units of the last wave are split into min(W / (U mod W), 4, key tiles / 4)
+ * ranges when that is at least 2 and U >= W (bf16, non-causal only).
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (as fa_fwd_ex).
+ */
+fa_status fa_fwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int resident_ctas,
+                      int* n_full, int* n_tail, int* splits);
+
+/*
+ * fa_fwd_ex with scratch for the tail of the schedule. The forward runs one
+ * CTA per (batch*head, 256-query block) unit, one CTA per SM; when the last
+ * wave of CTAs is only partly filled, its units are split into 2-4 key
+ * ranges, each range runs as a CTA of its own and leaves a partial result in
+ * the scratch, and a second kernel on the same stream combines the parts by
+ * their maxima and sums ("Lesson 1: FlashAttention core idea" §3). O and LSE
+ * are the same attention (other rounding order within fp32).
+ *   workspace       : device scratch of >= fa_fwd_workspace_bytes() bytes,
+ *                     256-byte aligned, contents on entry irrelevant, used by
+ *                     one call at a time (stream-ordered); NULL (or a
+ *                     problem that needs none) runs the plain schedule.
+ * Errors: as fa_fwd_ex, plus FA_ERR_INVALID_ARG for a non-NULL workspace
+ * that is too small or misaligned.
+ */
+fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                    float scale, int flags, fa_dtype dt, void* stream);
+
+/*
  * Variable-length batch (packed layout, no padding): B sequences of
  * different lengths, sequence b holding rows cu_seqlens[b] ..
  * cu_seqlens[b+1]-1 of the packed tensors. Each sequence is attended to

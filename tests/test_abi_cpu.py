@@ -5,6 +5,7 @@ import ctypes
 import os
 
 import pytest
+import torch
 
 import exact_attention_30_gb300 as fa
 from exact_attention_30_gb300 import build as fa_build
@@ -127,6 +128,52 @@ def test_decode_plan_on_the_host(lib, B, H, nq, nk, slots):
     best = min(_plan_cost(B * H, nk, slots, t, tile)[0] for t in range(1, min(256, -(-nk // tile)) + 1)
                if -(-nk // _plan_cost(B * H, nk, slots, t, tile)[1]) == t)
     assert _plan_cost(B * H, nk, slots, s, tile)[0] == best
+
+
+def _tail_makespan(units, slots, n_full, n_tail, splits):
+    """Waves of whole-unit time: full waves, then the tail at 1/splits each
+    (every tail range runs in the same wave when n_tail * splits <= slots)."""
+    assert n_full % slots == 0 and n_tail * splits <= slots
+    return n_full // slots + (1.0 / splits if n_tail else 0.0)
+
+
+@pytest.mark.parametrize("B,H,N,d,slots", [
+    (2, 16, 4096, 128, 152), (1, 32, 16384, 128, 152), (4, 16, 1024, 64, 152),
+    (1, 10, 4096, 128, 152), (1, 10, 4000, 64, 152), (1, 4, 4096, 128, 152),
+    (1, 200, 1024, 128, 152), (1, 200, 256, 128, 152), (3, 7, 777, 64, 148), (1, 1, 1, 128, 152)])
+def test_forward_tail_split_plan_on_the_host(lib, B, H, N, d, slots):
+    """The forward's tail split covers every unit once, splits only the last,
+    partly filled wave (never with fewer than four key tiles per range, at
+    most four ranges, all of them in one wave) and never lengthens the
+    schedule; causal and fp32 problems are not split."""
+    units = B * H * -(-N // 256)
+    n_kv = -(-N // 128)
+    nf, nt, sp = fa.fa_fwd_plan(B, H, N, d, resident_ctas=slots)
+    assert nf + nt == units and sp >= 1 and (sp == 1) == (nt == 0)
+    if sp > 1:
+        assert nt == units % slots and units >= slots
+        assert 2 <= sp <= 4 and n_kv // sp >= 4 and nt * sp <= slots
+        assert sp == min(slots // nt, 4, n_kv // 4)
+        whole = -(-units // slots)
+        assert _tail_makespan(units, slots, nf, nt, sp) < whole
+    else:
+        rem = units % slots
+        assert rem == 0 or units < slots or min(slots // rem, 4, n_kv // 4) < 2
+    assert fa.fa_fwd_plan(B, H, N, d, causal=True, resident_ctas=slots) == (units, 0, 1)
+    assert fa.fa_fwd_plan(B, H, N, d, dtype=torch.float32, resident_ctas=slots) == (units, 0, 1)
+
+
+def test_forward_workspace_entry_points_without_a_gpu(lib):
+    # no device: nothing is split, so no scratch is asked for
+    assert lib.fa_fwd_workspace_bytes(2, 16, 4096, 128, 0, fa.FA_BF16) == 0
+    assert lib.fa_fwd_workspace_bytes(2, 16, 4096, 96, 0, fa.FA_BF16) == 0
+    assert lib.fa_fwd_workspace_bytes(2, 16, 4096, 128, 4, fa.FA_BF16) == 0
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert lib.fa_fwd_ws(*ok, None, 0, 1, 2, 64, 64, 0.125, 4, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_ws(*ok, None, 0, 0, 2, 64, 64, 0.125, 0, fa.FA_BF16, None) == fa.FA_ERR_INVALID_ARG
+    nf = ctypes.c_int()
+    assert lib.fa_fwd_plan(1, 1, 64, 64, 0, fa.FA_BF16, -1, ctypes.byref(nf), ctypes.byref(nf),
+                           ctypes.byref(nf)) == fa.FA_ERR_INVALID_ARG
 
 
 def test_ex_and_varlen_entry_points_reject_bad_arguments_before_launch(lib):
