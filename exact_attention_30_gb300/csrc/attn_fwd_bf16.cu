@@ -650,28 +650,28 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
 // idea" §3: partial softmaxes merge through their maxima and sums): row r
 // gets O = sum_p w_p O_p / sum_p w_p with w_p = 2^(L_p - max L), and LSE =
 // (max L + log2 sum_p w_p) ln 2. Warp-wide rows (lanes along d, coalesced),
-// four rows per warp with every part's loads in flight.
-template <int D>
+// 16 / S rows per warp with every part's loads in flight (S = a.splits).
+template <int D, int S>
 __global__ void __launch_bounds__(256) fwd_tail_merge_kernel(const __grid_constant__ FwdArgs a) {
   constexpr int PER = D / 32;  // floats of a row per lane
-  constexpr int RPW = 4;       // rows per warp
+  constexpr int RPW = 16 / S;  // rows per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows_unit = 256;
   const int qblocks = (a.seq.N + rows_unit - 1) / rows_unit;
   const long long r_first = (long long)blockIdx.x * (8 * RPW) + warp * RPW;  // merged row: tail unit * 256 + row
-  float lp[RPW][kMaxTailSplits];
-  float x[RPW][kMaxTailSplits][PER];
+  float lp[RPW][S];
+  float x[RPW][S][PER];
 #pragma unroll
   for (int i = 0; i < RPW; ++i) {
     const long long mr = r_first + i;
     const long long tu = mr / rows_unit, ru = mr - tu * rows_unit;
 #pragma unroll
-    for (int p = 0; p < kMaxTailSplits; ++p) {
+    for (int p = 0; p < S; ++p) {
       lp[i][p] = -INFINITY;
 #pragma unroll
       for (int e = 0; e < PER; ++e) x[i][p][e] = 0.f;
-      if (p < a.splits && tu < a.n_tail) {
-        const size_t pr = (size_t)(tu * a.splits + p) * rows_unit + ru;
+      if (tu < a.n_tail) {
+        const size_t pr = (size_t)(tu * S + p) * rows_unit + ru;
         lp[i][p] = a.Lpart[pr];
         const float* src = a.Opart + pr * D + lane * PER;
         if constexpr (PER == 4) {
@@ -695,11 +695,11 @@ __global__ void __launch_bounds__(256) fwd_tail_merge_kernel(const __grid_consta
     if (row >= a.seq.N) continue;
     float L = -INFINITY;
 #pragma unroll
-    for (int p = 0; p < kMaxTailSplits; ++p) L = fmaxf(L, lp[i][p]);
-    float w[kMaxTailSplits], wsum = 0.f;
+    for (int p = 0; p < S; ++p) L = fmaxf(L, lp[i][p]);
+    float w[S], wsum = 0.f;
 #pragma unroll
-    for (int p = 0; p < kMaxTailSplits; ++p) {
-      w[p] = exp2f(lp[i][p] - L);  // 0 for the parts past a.splits
+    for (int p = 0; p < S; ++p) {
+      w[p] = exp2f(lp[i][p] - L);
       wsum += w[p];
     }
     const float inv_w = 1.f / wsum;
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(256) fwd_tail_merge_kernel(const __grid_consta
     for (int e = 0; e < PER; ++e) {
       float acc = 0.f;
 #pragma unroll
-      for (int p = 0; p < kMaxTailSplits; ++p) acc = fmaf(w[p], x[i][p][e], acc);
+      for (int p = 0; p < S; ++p) acc = fmaf(w[p], x[i][p][e], acc);
       y[e] = acc * inv_w;
     }
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) + (size_t)bh * (size_t)a.seq.plane_stride +
@@ -745,7 +745,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, int BH, cudaStream_t st) {
   cudaError_t e2 = cudaGetLastError();
   if (e2 != cudaSuccess || a.splits == 1) return e2;
   const long long merge_rows = (long long)a.n_tail * C::BM * C::QT;
-  fwd_tail_merge_kernel<D><<<(unsigned)((merge_rows + 31) / 32), 256, 0, st>>>(a);
+  auto blocks = [&](int rows_per_warp) {
+    return (unsigned)((merge_rows + 8 * rows_per_warp - 1) / (8 * rows_per_warp));
+  };
+  if (a.splits == 2) fwd_tail_merge_kernel<D, 2><<<blocks(8), 256, 0, st>>>(a);
+  else if (a.splits == 3) fwd_tail_merge_kernel<D, 3><<<blocks(5), 256, 0, st>>>(a);
+  else fwd_tail_merge_kernel<D, 4><<<blocks(4), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

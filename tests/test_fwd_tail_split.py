@@ -56,7 +56,7 @@ def _unit_heads(B, H, N, n_full):
     return [divmod(0, H)] + [divmod(bh, H) for bh in split_heads]
 
 
-@pytest.mark.parametrize("B,H,N,d", [(1, 10, 4096, 128), (1, 10, 4000, 64), (1, 13, 3001, 128),
+@pytest.mark.parametrize("B,H,N,d", [(1, 10, 4096, 128), (1, 12, 4096, 128), (1, 10, 4000, 64), (1, 13, 3001, 128),
                                      (2, 16, 4096, 128), (1, 200, 1024, 64)])
 def test_split_tail_matches_oracle_and_plain_schedule(B, H, N, d):
     n_full, n_tail, splits = fa.fa_fwd_plan(B, H, N, d)
