@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Throughput of the fused exact-attention hot path on one (or N) GB300.
 
-One step = the whole path on one synthetic batch: fa_fwd (O, LSE) then the
-three backward stages (preprocess, recompute main kernel, dQ convert), bf16,
+One step = the whole path on one synthetic batch: fa_fwd (O, LSE; with the
+tail of its schedule split and merged by a second kernel when the last wave of
+CTAs is partly filled) then the three backward stages (preprocess, recompute
+main kernel, dQ convert), bf16,
 B=2 H=16 N=4096 d=128, non-causal, inputs i.i.d. N(0,1) rounded to bf16.
 FLOPs per step: 4*B*H*N^2*d (forward) + 2.5x that (backward).
 
@@ -343,6 +345,11 @@ def run_gpu(args):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     causal = bool(args.causal)
+    # the forward's scratch for splitting a partly filled last wave (none when
+    # nothing is split); the step then launches the merge kernel as well
+    fws_bytes = fa.fa_fwd_workspace_bytes(B, H, N, D, causal=causal)
+    fws = torch.empty(fws_bytes, dtype=torch.uint8, device=dev) if fws_bytes else None
+    launches_per_step = 4 + (1 if fws_bytes else 0)
 
     def bwd_stage(stage):
         fa.fa_bwd_stage(stage, q, k, v, o, do, lse, scale, workspace=ws, dq=dq, dk=dk, dv=dv,
@@ -351,7 +358,7 @@ def run_gpu(args):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        fa.fa_fwd(q, k, v, scale, out=o, lse=lse, causal=causal)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse, causal=causal, workspace=fws)
         if ev is not None:
             ev[1].record(stream)
         bwd_stage(fa.FA_BWD_PREPROCESS)
@@ -441,7 +448,7 @@ def run_gpu(args):
                 qq, kk, vv, dd = dev_in[b]
                 oo, ll = dev_o[b]
                 g1, g2, g3 = dev_out[b]
-                fa.fa_fwd(qq, kk, vv, scale, out=oo, lse=ll, causal=causal)
+                fa.fa_fwd(qq, kk, vv, scale, out=oo, lse=ll, causal=causal, workspace=fws)
                 fa.fa_bwd(qq, kk, vv, oo, dd, ll, scale, workspace=ws2[b], dq=g1, dk=g2, dv=g3,
                           causal=causal)
                 done_cmp[b] = torch.cuda.Event()
@@ -501,7 +508,8 @@ def run_gpu(args):
                      "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
                      "algorithmic_flops_per_launch": BWD_FLOPS},
         "components": {
-            "fwd": {"kernel": f"fwd_bf16_kernel<{D}>", "ms": fwd_avg,
+            "fwd": {"kernel": f"fwd_bf16_kernel<{D}>" + (" + fwd_tail_merge_kernel" if fws_bytes else ""),
+                    "ms": fwd_avg,
                     "tflops": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12,
                     "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak},
             "bwd_preprocess": {"ms": mean(pre_ms)},
@@ -516,7 +524,7 @@ def run_gpu(args):
                 "ms_per_step": e2e_ms, "pipelined": "2 buffer sets, input/compute/result streams",
                 "h2d_bytes_per_step": 4 * nbytes,
                 "d2h_bytes_per_step": 3 * nbytes},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     if causal:
