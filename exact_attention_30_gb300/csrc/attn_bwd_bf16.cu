@@ -677,8 +677,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
       }
     }
-    // every bulk reduction must be complete before the block exits
-    if (lane == 0) bulk_wait_group_all();
+    // every bulk reduction must have read its staging block before the CTA
+    // exits; the additions land before the kernel ends
+    if (lane == 0) bulk_wait_group_read<0>();
   }
 
   tc_fence_before();

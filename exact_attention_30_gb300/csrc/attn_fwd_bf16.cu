@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) tma_store_2d(&a.tmOpart, smem_u32(stage + q * 16384), q * 32, prow0);
         bulk_commit_group();
-        bulk_wait_group_all();
+        bulk_wait_group_read<0>();  // the staging read; the writes land before the kernel ends
       }
     } else if (ok) {
       tc_fence_after();
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
           for (int c = 0; c < C::CH; ++c)
             tma_store_3d(&a.tmO, smem_u32(stage + c * C::CHUNK_BYTES), c * 64, y0 + q0 + t * C::BM, plane);
           bulk_commit_group();
-          bulk_wait_group_all();  // written, and the slot read, before the CTA exits
+          bulk_wait_group_read<0>();  // the slot read before the CTA exits; the writes land before the kernel ends
         }
       } else {
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) + seq_row_offset(a.seq, sv, row);
