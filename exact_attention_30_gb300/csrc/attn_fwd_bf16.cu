@@ -14,9 +14,11 @@
 //               and one elected lane issues every tcgen05.mma:
 //                 S_t = Q_t K_j^T   (SS form, fp32 accumulator in TMEM)
 //                 O_t += P_t V_j    (TS form: P read from TMEM, V from smem)
-//               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the
-//               tensor core works on one query tile while the softmax warps
-//               work on the other.
+//               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) (d = 128),
+//               so the tensor core works on one query tile while the softmax
+//               warps work on the other; at d = 64, where P has TMEM columns
+//               of its own, S_t(j+1) goes before PV_t(j), as soon as the
+//               softmax has read S_t(j).
 //   warps 4-7   softmax for query tile 0, one thread per row (TMEM lane);
 //   warps 8-11  softmax for query tile 1.
 // Online softmax ("Lesson 1" §3) in the log2 domain: x = s * scale*log2(e),
@@ -29,7 +31,13 @@
 // next P V product is issued. P is rounded to bf16 and written over the S
 // columns it came from (d = 128), or into columns of its own (d = 64, where
 // TMEM has room); either way it is the A operand of the TS MMA.
-// Epilogue: O / l to bf16, LSE = (m_ref + log2 l) * ln 2, rows >= N skipped.
+// Epilogue: O / l to bf16 through the tile's Q slot and TMA tensor stores,
+// LSE = (m_ref + log2 l) * ln 2, rows >= N skipped.
+//
+// Grid (non-causal): one CTA per unit (batch*head, 256-row block), head-major.
+// When the last wave of CTAs is only partly filled, the caller's scratch lets
+// its units run as 2-4 key ranges each; a range writes its normalised fp32 O
+// and base-2 LSE, and fwd_tail_merge_kernel combines the ranges afterwards.
 //
 // Sequences: a CTA works on one sequence of the SeqArgs layout (fixed length,
 // or one entry of a packed variable-length batch); keys past the sequence's
