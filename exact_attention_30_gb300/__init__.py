@@ -340,7 +340,7 @@ def fa_decode_plan(B: int, H: int, Nq: int, Nk: int, d: int, resident_ctas: int 
 
 
 def fa_decode(q, k, v, scale: float | None = None, out=None, lse=None, workspace=None):
-    """KV-cache decode: q [B,H,Nq,d] (Nq <= 8) against k, v [B,H,Nk,d], bf16.
+    """KV-cache decode: q [B,H,Nq,d] (Nq <= 16) against k, v [B,H,Nk,d], bf16.
 
     Returns (O like q, LSE [B,H,Nq] float32).
     """
