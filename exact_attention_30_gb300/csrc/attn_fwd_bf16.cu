@@ -79,7 +79,7 @@ struct FwdCfg {
   static constexpr int OFF_K = OFF_Q + QT * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * TILE_BYTES;
-  static constexpr int NBAR = 1 + 4 * STAGES + 4 * QT + 1;
+  static constexpr int NBAR = QT + 4 * STAGES + 4 * QT + 1;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
   static constexpr int THREADS = 384;
@@ -166,10 +166,10 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
   // barrier indices
   const uint32_t bar0 = smem_u32(bars);
   auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  const int B_QFULL = 0;
-  const int B_KFULL = 1, B_VFULL = 1 + C::STAGES, B_KEMPTY = 1 + 2 * C::STAGES,
-            B_VEMPTY = 1 + 3 * C::STAGES;
-  const int B_SFULL = 1 + 4 * C::STAGES, B_PFULL = B_SFULL + C::QT, B_ODONE = B_PFULL + C::QT;
+  const int B_QFULL = 0;  // + query tile: each Q tile has its own barrier
+  const int B_KFULL = C::QT, B_VFULL = C::QT + C::STAGES, B_KEMPTY = C::QT + 2 * C::STAGES,
+            B_VEMPTY = C::QT + 3 * C::STAGES;
+  const int B_SFULL = C::QT + 4 * C::STAGES, B_PFULL = B_SFULL + C::QT, B_ODONE = B_PFULL + C::QT;
   const int B_SFREE = B_ODONE + C::QT;  // S read by the softmax (own-P layout only)
   const int B_DRAIN = B_SFREE + C::QT;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
   const int plane = sv.plane;
 
   if (threadIdx.x == 0) {
-    mbar_init(BAR(B_QFULL), 1);
+    for (int t = 0; t < C::QT; ++t) mbar_init(BAR(B_QFULL + t), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(BAR(B_KFULL + s), 1);
       mbar_init(BAR(B_VFULL + s), 1);
@@ -249,11 +249,15 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       tma_prefetch_desc(&a.tmQ);
       tma_prefetch_desc(&a.tmK);
       tma_prefetch_desc(&a.tmV);
-      mbar_arrive_expect_tx(BAR(B_QFULL), C::QT * C::TILE_BYTES);
-      for (int t = 0; t < C::QT; ++t)
+      // Q tile 0, then K_0, then the other Q tiles: S_0(0) needs only the first two
+      auto load_q = [&](int t) {
+        mbar_arrive_expect_tx(BAR(B_QFULL + t), C::TILE_BYTES);
         for (int c = 0; c < C::CH; ++c)
-          tma_load_3d(sbase + C::OFF_Q + (t * C::CH + c) * C::CHUNK_BYTES, &a.tmQ, BAR(B_QFULL),
+          tma_load_3d(sbase + C::OFF_Q + (t * C::CH + c) * C::CHUNK_BYTES, &a.tmQ, BAR(B_QFULL + t),
                       c * 64, y0 + q0 + t * C::BM, plane);
+      };
+      load_q(0);
+      int q_loaded = 1;
       int last_k[C::STAGES], last_v[C::STAGES];  // last tile loaded into each slot
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) last_k[s] = last_v[s] = -1;
@@ -267,6 +271,8 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
           tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmK,
                       BAR(B_KFULL + s), c * 64, y0 + (kt0 + j) * C::BN, plane);
         last_k[s] = j;
+        if (j == 0)
+          for (; q_loaded < C::QT; ++q_loaded) load_q(q_loaded);
         if (!mbar_wait(BAR(B_VEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(BAR(B_VFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::CH; ++c)
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         last_v[s] = j;
       }
       // drain: the last load issued into each slot must have landed before exit
-      mbar_wait(BAR(B_QFULL), 0, a.status, a.wait_limit_ns);
+      for (int t = 0; t < q_loaded; ++t) mbar_wait(BAR(B_QFULL + t), 0, a.status, a.wait_limit_ns);
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) {
         if (last_k[s] >= 0)
@@ -320,15 +326,14 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       auto wait = [&](int b, uint32_t parity) {
         return mbar_wait_warp(BAR(b), parity, a.status, a.wait_limit_ns);
       };
-      bool ok = wait(B_QFULL, 0) && wait(B_KFULL + 0, 0);
-      if (ok) {
+      bool ok = wait(B_QFULL + 0, 0) && wait(B_KFULL + 0, 0);
+      for (int t = 0; ok && t < C::QT; ++t) {
+        if (t > 0 && !wait(B_QFULL + t, 0)) { ok = false; break; }
         tc_fence_after();
-        for (int t = 0; t < C::QT; ++t) {
-          issue_s(t, 0);
-          mma_commit(BAR(B_SFULL + t), leader);
-        }
-        mma_commit(BAR(B_KEMPTY + 0), leader);
+        issue_s(t, 0);
+        mma_commit(BAR(B_SFULL + t), leader);
       }
+      if (ok) mma_commit(BAR(B_KEMPTY + 0), leader);
       for (int j = 0; ok && j < n_max; ++j) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
         const int s = j % C::STAGES;
