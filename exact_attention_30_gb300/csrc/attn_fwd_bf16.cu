@@ -7,7 +7,7 @@
 // with S and P held only in tensor memory (TMEM) and registers.
 //
 // CTA = one (batch*head, 256-row query block) = two 128-row query tiles.
-// Warp roles (12 warps):
+// Warp roles (10 warps):
 //   warp 0      TMA producer: Q tiles once, then K_j / V_j through a ring of
 //               STAGES shared-memory slots (full/empty mbarrier pairs).
 //   warp 1      TMEM allocation; the converged warp runs the MMA schedule
@@ -19,8 +19,8 @@
 //               warps work on the other; at d = 64, where P has TMEM columns
 //               of its own, S_t(j+1) goes before PV_t(j), as soon as the
 //               softmax has read S_t(j).
-//   warps 4-7   softmax for query tile 0, one thread per row (TMEM lane);
-//   warps 8-11  softmax for query tile 1.
+//   warps 2-5   softmax for query tile 0, one thread per row (TMEM lane);
+//   warps 6-9   softmax for query tile 1.
 // Online softmax ("Lesson 1" §3) in the log2 domain: x = s * scale*log2(e),
 // p = 2^(x - m_ref), l = l * 2^(m_ref_old - m_ref) + rowsum(p). The reference
 // max m_ref is only raised when the tile max exceeds it by more than
@@ -82,7 +82,11 @@ struct FwdCfg {
   static constexpr int NBAR = QT + 4 * STAGES + 4 * QT + 1;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1024-byte alignment
-  static constexpr int THREADS = 384;
+  // warps: 0 producer, 1 MMA, 2-5 and 6-9 the softmax warpgroups of query
+  // tiles 0 and 1 (any four consecutive warps cover the four TMEM lane
+  // quarters); 320 threads leave 200 registers per thread
+  static constexpr int SW0 = 2;
+  static constexpr int THREADS = 32 * (SW0 + 4 * QT);
   static constexpr uint32_t TMEM_COLS = 512;
   // TMEM columns: S_t at 128*t, O_t at 256 + D*t. With d = 64 the last 128
   // columns are free and hold P_t (64 columns of bf16 pairs each), so P can
@@ -133,7 +137,7 @@ __device__ __forceinline__ bool softmax_pass_own_p(uint32_t s_addr, uint32_t p_a
   tmem_ld32(s_addr, ra);
   tmem_ld_wait_dep(ra);
   // not unrolled: fully unrolled, ptxas batches the exponentials of all the
-  // chunks and runs out of registers at the 384-thread cap
+  // chunks and runs out of registers
 #pragma unroll 1
   for (int c = 0; c < 4; c += 2) {
     tmem_ld32(s_addr + 32 * (c + 1), rb);
@@ -156,7 +160,7 @@ __device__ __forceinline__ bool softmax_pass_own_p(uint32_t s_addr, uint32_t p_a
 }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fwd_bf16_kernel(const __grid_constant__ FwdArgs a) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -389,9 +393,9 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       mma_commit(BAR(B_DRAIN), leader);
       wait(B_DRAIN, 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= C::SW0) {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 4) >> 2;       // query tile of this warpgroup
+    const int t = (warp - C::SW0) >> 2;  // query tile of this warpgroup
     const int wq = warp & 3;             // TMEM lane quarter
     const int row_in_tile = wq * 32 + lane;
     const int row = q0 + t * C::BM + row_in_tile;  // within the sequence
@@ -578,7 +582,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
       }
       if (t == 0) named_bar_sync<2>(128);
       else named_bar_sync<3>(128);
-      if (ok && warp == 4 + 4 * t && lane == 0) {
+      if (ok && warp == C::SW0 + 4 * t && lane == 0) {
         const uint8_t* stage = smem + C::OFF_Q + t * (D * 512);
 #pragma unroll
         for (int q = 0; q < D / 32; ++q) tma_store_2d(&a.tmOpart, smem_u32(stage + q * 16384), q * 32, prow0);
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(384, 1) fwd_bf16_kernel(const __grid_constant_
         fence_proxy_async_smem();
         if (t == 0) named_bar_sync<2>(128);  // this tile's softmax warps
         else named_bar_sync<3>(128);
-        if (warp == 4 + 4 * t && lane == 0) {
+        if (warp == C::SW0 + 4 * t && lane == 0) {
 #pragma unroll
           for (int c = 0; c < C::CH; ++c)
             tma_store_3d(&a.tmO, smem_u32(stage + c * C::CHUNK_BYTES), c * 64, y0 + q0 + t * C::BM, plane);
