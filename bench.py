@@ -479,7 +479,11 @@ def run_gpu(args):
         return 0
 
     peaks, peak_src = read_peaks()
-    peak = peaks["bf16_tflops"]
+    # the dominant kernel is timed inside a long run of steps, under the
+    # power cap: its denominator is the sustained bf16 figure; the burst
+    # figure (a GEMM timed alone) is reported beside it
+    peak = peaks["bf16_tflops_sustained"]
+    burst = peaks["bf16_tflops"]
     mean = lambda xs: sum(xs) / len(xs)
     main_avg = mean(main_ms)
     achieved = BWD_FLOPS / (main_avg * 1e-3) / 1e12
@@ -505,15 +509,18 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}, independent batches, no collective"},
         "roofline": {"kernel": f"bwd_main_kernel<{D}>", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_source": f"{peak_src} bf16 burst",
+                     "traffic": traffic, "peak_source": f"{peak_src} bf16 sustained",
+                     "frac_of_burst_peak": achieved / burst, "burst_peak": burst,
                      "algorithmic_flops_per_launch": BWD_FLOPS},
         "components": {
             "fwd": {"kernel": f"fwd_bf16_kernel<{D}>" + (" + fwd_tail_merge_kernel" if fws_bytes else ""),
                     "ms": fwd_avg,
                     "tflops": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12,
-                    "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak},
+                    "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak,
+                    "frac_of_burst_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / burst},
             "bwd_preprocess": {"ms": mean(pre_ms)},
-            "bwd_main": {"ms": main_avg, "tflops": achieved, "frac_of_peak": achieved / peak},
+            "bwd_main": {"ms": main_avg, "tflops": achieved, "frac_of_peak": achieved / peak,
+                         "frac_of_burst_peak": achieved / burst},
             "bwd_dq_convert": {"ms": mean(conv_ms)},
             "bwd_total": {"ms": mean(pre_ms) + main_avg + mean(conv_ms),
                           "tflops": BWD_FLOPS / ((mean(pre_ms) + main_avg + mean(conv_ms)) * 1e-3) / 1e12},
@@ -759,9 +766,10 @@ def run_varlen(args):
         "components": {"fwd": {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12},
                        "bwd": {"ms": bwd_ms, "tflops": 2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12}},
         "roofline": {"kernel": "fwd_bf16_kernel + bwd stages (one step)", "bound": "tensor",
-                     "achieved": value, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": value / peaks["bf16_tflops"], "traffic": None,
-                     "peak_source": f"{src} bf16 burst"},
+                     "achieved": value, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": value / peaks["bf16_tflops_sustained"], "traffic": None,
+                     "peak_source": f"{src} bf16 sustained",
+                     "frac_of_burst_peak": value / peaks["bf16_tflops"], "burst_peak": peaks["bf16_tflops"]},
         "gpu_launches": 4 * args.steps,
     }
     print(json.dumps(line), flush=True)
