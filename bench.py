@@ -55,7 +55,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--heads", type=int, default=None,
                    help="override H (smaller profiling captures); the JSON line names the change")
-    p.add_argument("--op", default="attention", choices=["attention", "softmax", "decode"],
+    p.add_argument("--op", default="attention", choices=["attention", "softmax", "decode", "minilab"],
                    help="softmax: time the fused row softmax on the B*H*N x N score matrix of "
                         "the shape; decode: time KV-cache decode on --decode-workload (both "
                         "HBM-bound; not the headline line)")
@@ -691,7 +691,7 @@ def run_decode(args):
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None,
                      "peak_source": f"{src} copy bandwidth",
                      "algorithmic_bytes_per_launch": nbytes},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds, w)
@@ -777,10 +777,110 @@ def run_varlen(args):
     return 0
 
 
+def run_minilab(args):
+    """The mini-lab configuration (fp32, B=H=1, N=16, d=8): the forward's
+    latency per call. Device time between CUDA events around each call, and
+    end to end through the public API with the 1.5 KB of inputs copied in from
+    pinned host memory and O, LSE read back every call."""
+    import numpy as np
+    import torch
+
+    import exact_attention_30_gb300 as fa
+    from exact_attention_30_gb300.inputs import minilab_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.load_library()
+    q64, k64, v64 = minilab_inputs()
+    to_host = lambda a: torch.from_numpy(a.astype(np.float32)).reshape(1, 1, 16, 8).pin_memory()
+    qh, kh, vh = to_host(q64), to_host(k64), to_host(v64)
+    q, k, v = (t.to(dev) for t in (qh, kh, vh))
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 16), dtype=torch.float32, device=dev)
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    scale = 1 / math.sqrt(8)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = sorted(1e3 * a.elapsed_time(b) for a, b in ev)  # isolated calls: host submission included
+    # device time per call: 100 calls captured in a CUDA graph (no host work
+    # between them), the graph replayed args.steps // 100 times
+    per_graph = 100
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(per_graph):
+                fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+    stream.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    replays = max(1, args.steps // per_graph)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    med = 1e3 * e0.elapsed_time(e1) / (replays * per_graph)
+    # end to end: copy in, forward, read O and LSE back, every call
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        for dst, src in ((q, qh), (k, kh), (v, vh)):
+            dst.copy_(src, non_blocking=True)
+        fa.fa_fwd(q, k, v, scale, out=o, lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_us = 1e3 * e0.elapsed_time(e1) / args.steps
+    line = {
+        "metric": "mini-lab fp32 forward device time per call (calls replayed from a CUDA graph)",
+        "value": med, "unit": "us",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e-3,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "fp32 forward B=1 H=1 N=16 d=8 (default_rng(0) inputs)",
+                   "isolated_call_us": {"median": us[len(us) // 2], "p10": us[len(us) // 10],
+                                        "p90": us[(9 * len(us)) // 10],
+                                        "note": "CUDA events around one call on an idle stream, "
+                                                "host submission included"},
+                   "l2": "not flushed (1.5 KB of inputs)"},
+        "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": 3 * qh.numel() * 4,
+                "d2h_bytes_per_step": (oh.numel() + lh.numel()) * 4},
+        "gpu_launches": args.steps,
+    }
+    if not args.no_cpu_baseline:
+        from oracle import attention_fwd  # the baseline leg may run the oracle
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 2.0):
+            attention_fwd(q64, k64, v64, scale)
+            n += 1
+        cpu_us = 1e6 * (time.perf_counter() - t0) / n
+        line["cpu_baseline"] = {"value": cpu_us, "unit": "us", "cores": 1, "kind": "oracle",
+                                "sample": f"fp64 numpy oracle forward of the same 16 x 8 problem, {n} calls"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.op == "softmax":
         return run_softmax(args)
+    if args.op == "minilab":
+        return run_minilab(args)
     if args.varlen:
         return run_varlen(args)
     if args.op == "decode":
