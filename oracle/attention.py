@@ -56,8 +56,9 @@ Readings where the pages are silent (each also listed in the design notes):
 Pins (tests/test_oracle_pins.py): the worked example, the mini-lab agreement
 of naive and tiled paths, row-stochastic P, closed forms (N = 1, Q = 0, a
 dominant key, permutation and key-shift invariance), PyTorch's float64 CPU
-scaled_dot_product_attention + autograd, and central finite differences for
-the backward pass. No function here is "parity unpinned".
+scaled_dot_product_attention + autograd (per head, and batched over [B, H] for
+the ``*_batched`` wrappers, with a head subset left NaN), and central finite
+differences for the backward pass. No function here is "parity unpinned".
 """
 from __future__ import annotations
 

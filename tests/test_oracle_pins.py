@@ -12,9 +12,10 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import (attention_bwd, attention_fwd, attention_fwd_rows, merge_partials,
-                    online_softmax_stats, row_softmax, scores, split_kv_attention_fwd,
-                    tiled_attention_fwd, varlen_attention_bwd, varlen_attention_fwd)
+from oracle import (attention_bwd, attention_bwd_batched, attention_fwd, attention_fwd_batched,
+                    attention_fwd_rows, merge_partials, online_softmax_stats, row_softmax, scores,
+                    split_kv_attention_fwd, tiled_attention_fwd, varlen_attention_bwd,
+                    varlen_attention_fwd)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -392,3 +393,62 @@ def test_varlen_against_torch_sdpa_per_sequence(causal):
                 S = np.where(np.tril(np.ones_like(S, dtype=bool)), S, -np.inf)
             ref_lse = np.log(np.exp(S - S.max(1, keepdims=True)).sum(1)) + S.max(1)
             assert np.abs(LSE[h, s:e] - ref_lse).max() <= 1e-12
+
+
+# --- the [B, H, N, d] batch wrappers against the library's batched routine -----------
+
+def _torch_batch(B, H, N, d, dv, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, N, d, dtype=torch.float64, generator=g, requires_grad=True)
+    k = torch.randn(B, H, N, d, dtype=torch.float64, generator=g, requires_grad=True)
+    v = torch.randn(B, H, N, dv, dtype=torch.float64, generator=g, requires_grad=True)
+    do = torch.randn(B, H, N, dv, dtype=torch.float64, generator=g)
+    return q, k, v, do
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_wrappers_against_torch_batched_sdpa_float64(causal):
+    """Every (b, h) of the wrappers' output against torch's batched SDPA + autograd.
+
+    The heads differ (distinct seeded draws), so a swapped b/h index, a head
+    computed from another head's K or V, or dQ/dK/dV returned in the wrong
+    slot fails here. LSE is checked against its definition computed by torch.
+    """
+    B, H, N, d, dv, scale = 2, 3, 19, 8, 5, 0.3
+    q, k, v, do = _torch_batch(B, H, N, d, dv, 11 + causal)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale, is_causal=causal)
+    o.backward(do)
+    Q, K, V, dO = (t.detach().numpy() for t in (q, k, v, do))
+    O, LSE = attention_fwd_batched(Q, K, V, scale, causal=causal)
+    dQ, dK, dV = attention_bwd_batched(Q, K, V, dO, scale, causal=causal)
+    assert O.shape == (B, H, N, dv) and LSE.shape == (B, H, N)
+    assert np.abs(O - o.detach().numpy()).max() <= 1e-12
+    s = scale * torch.einsum("bhnd,bhmd->bhnm", q.detach(), k.detach())
+    if causal:
+        s = s.masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), -math.inf)
+    assert np.abs(LSE - torch.logsumexp(s, dim=-1).numpy()).max() <= 1e-12
+    for mine, ref in ((dQ, q.grad), (dK, k.grad), (dV, v.grad)):
+        assert mine.shape == tuple(ref.shape)
+        assert np.abs(mine - ref.numpy()).max() <= 1e-12
+
+
+def test_batched_wrappers_head_subset_leaves_the_rest_nan():
+    B, H, N, d = 2, 3, 9, 4
+    q, k, v, do = _torch_batch(B, H, N, d, d, 5)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=0.7)
+    o.backward(do)
+    Q, K, V, dO = (t.detach().numpy() for t in (q, k, v, do))
+    heads = [(1, 2), (0, 1)]
+    O, LSE = attention_fwd_batched(Q, K, V, 0.7, heads=heads)
+    grads = attention_bwd_batched(Q, K, V, dO, 0.7, heads=heads)
+    for b in range(B):
+        for h in range(H):
+            if (b, h) in heads:
+                assert np.abs(O[b, h] - o[b, h].detach().numpy()).max() <= 1e-12
+                assert np.isfinite(LSE[b, h]).all()
+                for mine, ref in zip(grads, (q.grad, k.grad, v.grad)):
+                    assert np.abs(mine[b, h] - ref[b, h].numpy()).max() <= 1e-12
+            else:
+                assert np.isnan(O[b, h]).all() and np.isnan(LSE[b, h]).all()
+                for mine in grads:
+                    assert np.isnan(mine[b, h]).all()
