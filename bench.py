@@ -122,6 +122,21 @@ def read_peaks():
         return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0), "fallback"
 
 
+# A timed region counts as "sustained" (the power-capped GEMM loop's figure)
+# only when it lasted at least this long and the clock sampler saw the power
+# cap active; anything shorter is a burst, judged against the burst GEMM.
+SUSTAINED_MIN_SECONDS = 2.0
+
+
+def bf16_peak(peaks, src, clocks, timed_seconds):
+    """(peak TFLOP/s, label) for a tensor-bound kernel timed over `timed_seconds`."""
+    capped = bool(clocks) and "sw_power_cap" in (clocks.get("reasons") or [])
+    if capped and timed_seconds >= SUSTAINED_MIN_SECONDS:
+        return peaks["bf16_tflops_sustained"], f"{src} bf16 sustained (timed {timed_seconds:.1f} s under sw_power_cap)"
+    why = "no power cap sampled" if not capped else f"timed region {timed_seconds:.2f} s < {SUSTAINED_MIN_SECONDS} s"
+    return peaks["bf16_tflops"], f"{src} bf16 burst ({why})"
+
+
 def read_traffic():
     """DRAM bytes per launch of the backward main kernel from the committed ncu
     summary, or None when the kernel source changed since it was captured."""
@@ -479,11 +494,11 @@ def run_gpu(args):
         return 0
 
     peaks, peak_src = read_peaks()
-    # the dominant kernel is timed inside a long run of steps, under the
-    # power cap: its denominator is the sustained bf16 figure; the burst
-    # figure (a GEMM timed alone) is reported beside it
-    peak = peaks["bf16_tflops_sustained"]
-    burst = peaks["bf16_tflops"]
+    # The denominator is the burst bf16 figure (a GEMM timed alone) unless the
+    # timed loop ran for seconds under the power cap; the other figure is
+    # reported beside it.
+    peak, peak_label = bf16_peak(peaks, peak_src, clocks, wall)
+    burst, sustained = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
     mean = lambda xs: sum(xs) / len(xs)
     main_avg = mean(main_ms)
     achieved = BWD_FLOPS / (main_avg * 1e-3) / 1e12
@@ -509,18 +524,22 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world}, independent batches, no collective"},
         "roofline": {"kernel": f"bwd_main_kernel<{D}>", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_source": f"{peak_src} bf16 sustained",
+                     "traffic": traffic, "peak_source": peak_label,
                      "frac_of_burst_peak": achieved / burst, "burst_peak": burst,
+                     "frac_of_sustained_peak": achieved / sustained, "sustained_peak": sustained,
+                     "timed_region_s": wall,
                      "algorithmic_flops_per_launch": BWD_FLOPS},
         "components": {
             "fwd": {"kernel": f"fwd_bf16_kernel<{D}>" + (" + fwd_tail_merge_kernel" if fws_bytes else ""),
                     "ms": fwd_avg,
                     "tflops": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12,
                     "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak,
-                    "frac_of_burst_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / burst},
+                    "frac_of_burst_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / burst,
+                    "frac_of_sustained_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / sustained},
             "bwd_preprocess": {"ms": mean(pre_ms)},
             "bwd_main": {"ms": main_avg, "tflops": achieved, "frac_of_peak": achieved / peak,
-                         "frac_of_burst_peak": achieved / burst},
+                         "frac_of_burst_peak": achieved / burst,
+                         "frac_of_sustained_peak": achieved / sustained},
             "bwd_dq_convert": {"ms": mean(conv_ms)},
             "bwd_total": {"ms": mean(pre_ms) + main_avg + mean(conv_ms),
                           "tflops": BWD_FLOPS / ((mean(pre_ms) + main_avg + mean(conv_ms)) * 1e-3) / 1e12},
@@ -691,7 +710,8 @@ def run_decode(args):
                      "frac": gbs / peaks["hbm_gbs"], "traffic": None,
                      "peak_source": f"{src} copy bandwidth",
                      "algorithmic_bytes_per_launch": nbytes},
-        "gpu_launches": args.steps,
+        # every fa_decode call launches two kernels: the split kernel and the combine kernel
+        "gpu_launches": 2 * args.steps,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds, w)
@@ -754,6 +774,7 @@ def run_varlen(args):
     step_flops = fwd_flops * 3.5
     value = step_flops / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
     peaks, src = read_peaks()
+    vpeak, vlabel = bf16_peak(peaks, src, None, (fwd_ms + bwd_ms) * 1e-3 * args.steps)
     line = {
         "metric": "variable-length attention fwd/bwd TFLOP/s (bf16)", "value": value, "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": fwd_ms + bwd_ms,
@@ -767,10 +788,11 @@ def run_varlen(args):
         "components": {"fwd": {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12},
                        "bwd": {"ms": bwd_ms, "tflops": 2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12}},
         "roofline": {"kernel": "fwd_bf16_kernel + bwd stages (one step)", "bound": "tensor",
-                     "achieved": value, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": value / peaks["bf16_tflops_sustained"], "traffic": None,
-                     "peak_source": f"{src} bf16 sustained",
-                     "frac_of_burst_peak": value / peaks["bf16_tflops"], "burst_peak": peaks["bf16_tflops"]},
+                     "achieved": value, "peak": vpeak, "unit": "TFLOP/s",
+                     "frac": value / vpeak, "traffic": None,
+                     "peak_source": vlabel,
+                     "frac_of_burst_peak": value / peaks["bf16_tflops"], "burst_peak": peaks["bf16_tflops"],
+                     "frac_of_sustained_peak": value / peaks["bf16_tflops_sustained"]},
         "gpu_launches": 4 * args.steps,
     }
     print(json.dumps(line), flush=True)
@@ -832,7 +854,7 @@ def run_minilab(args):
         graph.replay()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    med = 1e3 * e0.elapsed_time(e1) / (replays * per_graph)
+    mean_us = 1e3 * e0.elapsed_time(e1) / (replays * per_graph)  # mean over the replayed calls
     # end to end: copy in, forward, read O and LSE back, every call
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -847,8 +869,8 @@ def run_minilab(args):
     e2e_us = 1e3 * e0.elapsed_time(e1) / args.steps
     line = {
         "metric": "mini-lab fp32 forward device time per call (calls replayed from a CUDA graph)",
-        "value": med, "unit": "us",
-        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e-3,
+        "value": mean_us, "unit": "us",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_us * 1e-3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": "fp32 forward B=1 H=1 N=16 d=8 (default_rng(0) inputs)",
@@ -859,18 +881,29 @@ def run_minilab(args):
                    "l2": "not flushed (1.5 KB of inputs)"},
         "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": 3 * qh.numel() * 4,
                 "d2h_bytes_per_step": (oh.numel() + lh.numel()) * 4},
-        "gpu_launches": args.steps,
+        # one forward kernel per call: the isolated calls, the graph-replayed
+        # calls and the end-to-end calls are all timed
+        "gpu_launches": args.steps + replays * per_graph + args.steps,
+        "launches_timed": {"isolated": args.steps, "graph_replayed": replays * per_graph,
+                           "end_to_end": args.steps},
     }
     if not args.no_cpu_baseline:
         from oracle import attention_fwd  # the baseline leg may run the oracle
         t0 = time.perf_counter()
         n = 0
         while time.perf_counter() - t0 < min(args.cpu_seconds, 2.0):
-            attention_fwd(q64, k64, v64, scale)
+            O_ref, L_ref = attention_fwd(q64, k64, v64, scale)
             n += 1
         cpu_us = 1e6 * (time.perf_counter() - t0) / n
+        # the last end-to-end call's O and LSE (already in host memory) against
+        # the oracle's result of the same problem, at the fp32 tolerance
+        err = max(float(np.abs(oh.reshape(16, 8).numpy() - O_ref).max()),
+                  float(np.abs(lh.reshape(16).numpy() - L_ref).max()))
+        if not err <= 1e-5:
+            raise RuntimeError(f"mini-lab forward differs from the oracle by {err:.3g} (> 1e-5)")
         line["cpu_baseline"] = {"value": cpu_us, "unit": "us", "cores": 1, "kind": "oracle",
-                                "sample": f"fp64 numpy oracle forward of the same 16 x 8 problem, {n} calls"}
+                                "sample": f"fp64 numpy oracle forward of the same 16 x 8 problem, {n} calls",
+                                "max_abs_diff_vs_gpu": err}
     print(json.dumps(line), flush=True)
     return 0
 

@@ -10,7 +10,7 @@ CUDA kernels; there is no CPU path. If the shared library has not been built
 
     o, lse = fa_fwd(q, k, v, scale)                 # q,k,v: [B,H,N,d] cuda
     dq, dk, dv = fa_bwd(q, k, v, o, do, lse, scale)
-    o, lse = fa_decode(q_new, k_cache, v_cache, scale)   # q_new: [B,H,Nq<=8,d]
+    o, lse = fa_decode(q_new, k_cache, v_cache, scale)   # q_new: [B,H,Nq<=16,d]
     o, lse = fa_fwd(q, k, v, causal=True)            # causal self-attention
     o, lse = fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen)   # packed [total,H,d]
 """

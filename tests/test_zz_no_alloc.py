@@ -23,14 +23,21 @@ pytestmark = pytest.mark.gpu
 
 
 def _noalloc(lib, q, k, v, o, do, lse, scale, dtype_code):
+    """One fa_bwd_noalloc call through the C ABI; returns (dQ, dK, dV) and the
+    change in the device's free memory across the call itself (the outputs
+    are allocated before the first reading)."""
     B, H, N, d = q.shape
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
     rc = lib.fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
                             ctypes.c_float(scale), dtype_code,
                             torch.cuda.current_stream().cuda_stream)
     assert rc == fa.FA_OK, fa.fa_status_string(rc)
-    return dq, dk, dv
+    assert fa.fa_check_device_status() == fa.FA_OK
+    free1 = torch.cuda.mem_get_info()[0]
+    return (dq, dk, dv), free0 - free1
 
 
 @pytest.mark.parametrize("B,H,N,d", [(1, 4, 1000, 128), (2, 3, 333, 64)])
@@ -40,9 +47,10 @@ def test_bf16_noalloc_matches_fa_bwd_twice(B, H, N, d):
     scale = 1 / math.sqrt(d)
     o, lse = fa.fa_fwd(q, k, v, scale)
     ref = fa.fa_bwd(q, k, v, o, do, lse, scale)
-    for _ in range(2):
-        got = _noalloc(lib, q, k, v, o, do, lse, scale, fa.FA_BF16)
-        assert fa.fa_check_device_status() == fa.FA_OK
+    for call in range(2):
+        got, used = _noalloc(lib, q, k, v, o, do, lse, scale, fa.FA_BF16)
+        if call == 1:
+            assert used == 0  # the second call (module loaded, scratch address cached) allocates nothing
         for g, r in zip(got, ref):
             assert rel_max(g, r) <= TOL_BF16_GRAD
 
@@ -53,8 +61,10 @@ def test_f32_noalloc_matches_fa_bwd_twice():
     scale = 1 / math.sqrt(40)
     o, lse = fa.fa_fwd(q, k, v, scale)
     ref = fa.fa_bwd(q, k, v, o, do, lse, scale)
-    for _ in range(2):
-        got = _noalloc(lib, q, k, v, o, do, lse, scale, fa.FA_F32)
+    for call in range(2):
+        got, used = _noalloc(lib, q, k, v, o, do, lse, scale, fa.FA_F32)
+        if call == 1:
+            assert used == 0
         for g, r in zip(got, ref):
             assert max_abs(g, r) <= TOL_F32_ABS
 
