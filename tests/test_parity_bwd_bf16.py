@@ -14,7 +14,6 @@ import torch
 import exact_attention_30_gb300 as fa
 from exact_attention_30_gb300.inputs import WORKLOADS, random_qkv, workload_inputs
 from oracle import attention_bwd
-import numpy as np
 
 from parity_utils import TOL_BF16_GRAD, grad_within, rel_max, to64
 
@@ -48,11 +47,28 @@ def test_ragged_lengths(N, d):
     _check_heads(q, k, v, do, grads, scale, [(0, 0), (0, 1)])
 
 
+def _check_dq_rows(q, k, v, do, dq, scale, rows_per_head, seed):
+    """dQ on sampled query rows of every head. A query row's gradient depends on
+    that row alone (its own softmax and its own rowsum(dP o P)), so the oracle
+    run on a subset of rows gives exactly those rows of dQ. The sample always
+    holds the last row (ragged tail) and row 0."""
+    q64, k64, v64, do64, dq64 = to64(q), to64(k), to64(v), to64(do), to64(dq)
+    B, H, N, _ = q64.shape
+    rng = np.random.default_rng(seed)
+    for b in range(B):
+        for h in range(H):
+            rows = np.sort(rng.choice(N, size=min(rows_per_head, N), replace=False))
+            rows[0], rows[-1] = 0, N - 1
+            ref, _, _ = attention_bwd(q64[b, h][rows], k64[b, h], v64[b, h], do64[b, h][rows], scale)
+            assert rel_max(dq64[b, h][rows], ref) <= TOL_BF16_GRAD, (b, h, rel_max(dq64[b, h][rows], ref))
+
+
 def test_workload_bwd_2x16x4096x128():
     w = WORKLOADS["bwd_bf16_2x16x4096x128"]
     q, k, v, do = workload_inputs(w)
     grads = _run(q, k, v, do, w.scale)
-    _check_heads(q, k, v, do, grads, w.scale, [(0, 0), (1, 15), (1, 3)])
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]  # every head, whole
+    _check_heads(q, k, v, do, grads, w.scale, heads)
 
 
 def test_workload_bwd_1x32x16384x128_with_big_keys():
@@ -60,6 +76,7 @@ def test_workload_bwd_1x32x16384x128_with_big_keys():
     q, k, v, do = workload_inputs(w)
     grads = _run(q, k, v, do, w.scale)
     _check_heads(q, k, v, do, grads, w.scale, [(0, 0), (0, 31)])
+    _check_dq_rows(q, k, v, do, grads[0], w.scale, rows_per_head=48, seed=3)
 
 
 def test_dk_dv_deterministic_and_dq_close():
