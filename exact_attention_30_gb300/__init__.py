@@ -63,6 +63,9 @@ _SIGNATURES = {
     "fa_decode_plan": (_ci, [_ci, _ci, _ci, _ci, _ci, _ci, ctypes.POINTER(_ci), ctypes.POINTER(_ci)]),
     "fa_check_device_status": (_ci, [_vp]),
     "fa_debug_timeout_probe": (_ci, [ctypes.c_longlong, _vp]),
+    "fa_debug_fwd_skip_load": (_ci, [_vp] * 5 + [_ci, _ci, _ci, _ci, _cf, _ci, ctypes.c_longlong, _vp]),
+    "fa_debug_bwd_skip_load": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci,
+                                                  ctypes.c_longlong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_ci]),
     "fa_version": (_ci, []),
 }

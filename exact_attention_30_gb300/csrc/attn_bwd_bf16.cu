@@ -281,11 +281,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         const int s = i % C::QSTAGES;
         const uint32_t ph = (i / C::QSTAGES) & 1;
         if (!mbar_wait(BAR(B_QEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(BAR(B_QFULL + s), C::TILE);
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
-                      c * 64, y0 + (i_begin + i) * C::BQ, plane);
-        last[s] = i;
+        if (i != a.debug_skip_q) {
+          mbar_arrive_expect_tx(BAR(B_QFULL + s), C::TILE);
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
+                        c * 64, y0 + (i_begin + i) * C::BQ, plane);
+          last[s] = i;
+        }
       }
       mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns);
 #pragma unroll
@@ -303,7 +305,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     // sequence, so that P = 0 there. Lane 0 issues the dO tile loads.
     const bool stat_bulk = a.seq.cu_seqlens == nullptr;  // rows 16-byte aligned, padded
     if (lane == 0) tma_prefetch_desc(&a.tmdO);
-    int last = -1;  // lane 0: last dO tile issued
+    int last = -1;       // lane 0: last dO tile issued
+    int last_stat = -1;  // lane 0: last statistics tile issued by bulk copies
     for (int i = 0; i < n_it; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       {
@@ -321,6 +324,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                       BAR(B_STFULL + t));
             bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES + C::BQ * 4, a.Drow + ws_row0 + q_row,
                       C::BQ * 4, BAR(B_STFULL + t));
+            last_stat = i;
           }
         } else {
           const size_t row0 = ws_row0 + (size_t)q_row + 4 * lane;
@@ -353,9 +357,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       __syncwarp();
     }
     if (lane == 0) {
-      // the last dO load issued into each slot must have landed before exit
+      // the last dO and statistics copies issued into each slot must have
+      // landed before exit (after an abort nobody else waits for them)
       for (int i = last - C::DOSTAGES + 1 < 0 ? 0 : last - C::DOSTAGES + 1; i <= last; ++i)
         mbar_wait(BAR(B_DOFULL + i % C::DOSTAGES), (i / C::DOSTAGES) & 1, a.status, a.wait_limit_ns);
+      for (int i = last_stat - C::STATSTAGES + 1 < 0 ? 0 : last_stat - C::STATSTAGES + 1; i <= last_stat; ++i)
+        mbar_wait(BAR(B_STFULL + i % C::STATSTAGES), (i / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
     }
     __syncwarp();
   } else if (warp == 1) {

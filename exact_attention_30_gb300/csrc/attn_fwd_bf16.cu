@@ -270,11 +270,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fwd_bf16_kernel(const _
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
         if (!mbar_wait(BAR(B_KEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(BAR(B_KFULL + s), C::TILE_BYTES);
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmK,
-                      BAR(B_KFULL + s), c * 64, y0 + (kt0 + j) * C::BN, plane);
-        last_k[s] = j;
+        if (j != a.debug_skip_kv) {
+          mbar_arrive_expect_tx(BAR(B_KFULL + s), C::TILE_BYTES);
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_3d(sbase + C::OFF_K + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &a.tmK,
+                        BAR(B_KFULL + s), c * 64, y0 + (kt0 + j) * C::BN, plane);
+          last_k[s] = j;
+        }
         if (j == 0)
           for (; q_loaded < C::QT; ++q_loaded) load_q(q_loaded);
         if (!mbar_wait(BAR(B_VEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
@@ -550,15 +552,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1) fwd_bf16_kernel(const _
       const bool w = mbar_wait(BAR(B_ODONE + t), (n_own - 1) & 1, a.status, a.wait_limit_ns);
       ok = __all_sync(0xffffffffu, w);
     }
+    // Every warp that shares an epilogue barrier takes the same decision: a
+    // warp that gave up must not leave the others waiting at a barrier it
+    // never reaches. Split units: both tiles' warps (they stage into shared
+    // memory the other tile may still read); otherwise the tile's own four.
+    if (tail_unit >= 0) ok = named_bar_and<1>(256, ok);
+    else if (t == 0) ok = named_bar_and<2>(128, ok);
+    else ok = named_bar_and<3>(128, ok);
     if (!ok) *abort_flag = 1;
     if (tail_unit >= 0) {
       // One key part of a split unit: its normalised partial O (fp32) and
       // base-2 LSE go to the workspace; fwd_tail_merge_kernel, launched after
       // this kernel, combines the parts. Both tiles' products are complete
-      // past the first barrier, so all of shared memory is free: tile t
+      // past the barrier above, so all of shared memory is free: tile t
       // stages its rows in [OFF_Q + t * D * 512, ...) as 32-column boxes of
       // 128 rows in the TMA 128-byte swizzle, and one thread stores them.
-      named_bar_sync<1>(256);
       const int rows_unit = C::BM * C::QT;
       const int prow0 = (tail_unit * a.splits + part) * rows_unit + t * C::BM;  // tile's first workspace row
       if (ok) {

@@ -227,18 +227,27 @@ using namespace fa;
 
 namespace {
 
+// Bounded-wait limit of the test hooks, clamped to [1 us, 2 s].
+unsigned long long clamp_limit(long long limit_ns) {
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 2000000000ll) limit_ns = 2000000000ll;
+  return (unsigned long long)limit_ns;
+}
+
 // Tail split of the bf16 forward for this problem on the current device (only
 // fixed-length, non-causal problems are split; the others: one plain plan).
-FwdTailPlan fwd_tail_plan(const SeqArgs& sq, int BH, fa_dtype dt) {
+FwdTailPlan fwd_tail_plan(const SeqArgs& sq, int BH, int d, fa_dtype dt) {
   const long long qblocks = ((long long)sq.N + 255) / 256;
   const long long units = qblocks * BH;
+  (void)d;
   if (dt != FA_BF16 || sq.causal || sq.cu_seqlens) return FwdTailPlan{(int)units, 0, 1};
   return plan_fwd_tail(units, (sq.N + 127) / 128, fwd_slots());
 }
 
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE,
                    const SeqArgs& sq, int B, int d, float scale, fa_dtype dt, void* stream,
-                   void* workspace = nullptr, size_t workspace_bytes = 0) {
+                   void* workspace = nullptr, size_t workspace_bytes = 0, int debug_skip = -1,
+                   unsigned long long wait_limit_ns = kDefaultWaitLimitNs) {
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   const size_t al = dt == FA_BF16 ? 16 : 4;
   if (!aligned(Q, al) || !aligned(K, al) || !aligned(V, al) || !aligned(O, al) || !aligned(LSE, 4))
@@ -267,8 +276,9 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.BH = BH;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  a.wait_limit_ns = kDefaultWaitLimitNs;
-  FwdTailPlan plan = fwd_tail_plan(sq, BH, dt);
+  a.wait_limit_ns = wait_limit_ns;
+  a.debug_skip_kv = debug_skip;
+  FwdTailPlan plan = fwd_tail_plan(sq, BH, d, dt);
   const size_t need = fwd_tail_workspace_bytes(plan, d);
   if (workspace != nullptr && need > 0) {
     if (!aligned(workspace, 256) || workspace_bytes < need) return FA_ERR_INVALID_ARG;
@@ -290,7 +300,8 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
 fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                    void* workspace, size_t workspace_bytes, const SeqArgs& sq, int B, int d,
-                   float scale, fa_dtype dt, void* stream) {
+                   float scale, fa_dtype dt, void* stream, int debug_skip = -1,
+                   unsigned long long wait_limit_ns = kDefaultWaitLimitNs) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
     return FA_ERR_INVALID_ARG;
   const size_t al = dt == FA_BF16 ? 16 : 4;
@@ -342,7 +353,8 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
-  a.wait_limit_ns = kDefaultWaitLimitNs;
+  a.wait_limit_ns = wait_limit_ns;
+  a.debug_skip_q = debug_skip;
   return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -379,7 +391,7 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int flags, fa_dtype dt) {
   if (check_shape(B, H, N, d, 1.f, dt) != FA_OK || (flags & ~FA_CAUSAL)) return 0;
   const SeqArgs sq = fixed_seq(H, N, d, flags & FA_CAUSAL);
-  return fwd_tail_workspace_bytes(fwd_tail_plan(sq, B * H, dt), d);
+  return fwd_tail_workspace_bytes(fwd_tail_plan(sq, B * H, d, dt), d);
 }
 
 fa_status fa_fwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int resident_ctas,
@@ -392,7 +404,7 @@ fa_status fa_fwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int re
   const long long units = ((long long)N + 255) / 256 * B * H;
   FwdTailPlan p{(int)units, 0, 1};
   if (resident_ctas == 0)
-    p = fwd_tail_plan(sq, B * H, dt);
+    p = fwd_tail_plan(sq, B * H, d, dt);
   else if (dt == FA_BF16 && !(flags & FA_CAUSAL))
     p = plan_fwd_tail(units, (N + 127) / 128, resident_ctas);
   *n_full = p.n_full;
@@ -599,12 +611,34 @@ fa_status fa_check_device_status(void* stream) {
   return FA_ERR_CUDA;
 }
 
+fa_status fa_debug_fwd_skip_load(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 int B, int H, int N, int d, float scale, int skip_tile,
+                                 long long limit_ns, void* stream) {
+  const fa_status s = check_shape(B, H, N, d, scale, FA_BF16);
+  if (s != FA_OK) return s;
+  if (skip_tile < 1 || skip_tile >= (N + 127) / 128) return FA_ERR_INVALID_ARG;
+  return fwd_impl(Q, K, V, O, LSE, fixed_seq(H, N, d, false), B, d, scale, FA_BF16, stream, nullptr,
+                  0, skip_tile, clamp_limit(limit_ns));
+}
+
+fa_status fa_debug_bwd_skip_load(const void* Q, const void* K, const void* V, const void* O,
+                                 const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                 void* workspace, size_t workspace_bytes, int B, int H, int N,
+                                 int d, float scale, int skip_tile, long long limit_ns,
+                                 void* stream) {
+  const fa_status s = check_shape(B, H, N, d, scale, FA_BF16);
+  if (s != FA_OK) return s;
+  if (skip_tile < 1 || skip_tile >= (N + bwd_query_tile(d) - 1) / bwd_query_tile(d))
+    return FA_ERR_INVALID_ARG;
+  return bwd_impl(kStageAll, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes,
+                  fixed_seq(H, N, d, false), B, d, scale, FA_BF16, stream, skip_tile,
+                  clamp_limit(limit_ns));
+}
+
 fa_status fa_debug_timeout_probe(long long limit_ns, void* stream) {
-  if (limit_ns < 1000) limit_ns = 1000;
-  if (limit_ns > 2000000000ll) limit_ns = 2000000000ll;
   int* status = device_status_ptr();
   if (!status) return FA_ERR_CUDA;
-  return launch_timeout_probe(status, (unsigned long long)limit_ns,
+  return launch_timeout_probe(status, clamp_limit(limit_ns),
                               static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FA_OK
              : FA_ERR_CUDA;

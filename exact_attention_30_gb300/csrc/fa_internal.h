@@ -67,6 +67,10 @@ struct FwdArgs {
   float* Opart;        // fp32 [n_tail][splits][256][d]: normalised partial O
   float* Lpart;        // fp32 [n_tail][splits][256]: base-2 log-sum-exp of each part
   CUtensorMap tmOpart;  // Opart as 2-D (d, rows), 32 x 128 boxes, 128-byte swizzle
+  // Test hook (fa_debug_fwd_skip_load): the producer issues neither the load
+  // nor the expected-bytes arrival of this key tile (index within the CTA's
+  // range), so the consumers' bounded waits run out. -1: load everything.
+  int debug_skip_kv;
 };
 cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st);
 
@@ -104,6 +108,10 @@ struct BwdArgs {
   float scale_log2;
   int* status;
   unsigned long long wait_limit_ns;
+  // Test hook (fa_debug_bwd_skip_load): the producer issues neither the load
+  // nor the expected-bytes arrival of the Q tile of this iteration, so the
+  // consumers' bounded waits run out. -1: load everything.
+  int debug_skip_q;
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
 // Row padding used by the bf16 backward workspace: ws_rows = roundup(total, 128)

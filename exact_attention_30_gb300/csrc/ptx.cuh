@@ -91,6 +91,21 @@ __device__ __forceinline__ void named_bar_sync(int count) {
   static_assert(ID >= 1 && ID <= 15, "named barrier id");
   asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
 }
+// Barrier ID (1..15) among `count` threads of the block that also reduces a
+// predicate: every participating thread gets the AND of all their `pred`s, so
+// a decision taken on the result is the same in every participating warp.
+template <int ID>
+__device__ __forceinline__ bool named_bar_and(int count, bool pred) {
+  static_assert(ID >= 1 && ID <= 15, "named barrier id");
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(ID), "r"(count)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -319,6 +319,34 @@ fa_status fa_check_device_status(void* stream);
  */
 fa_status fa_debug_timeout_probe(long long limit_ns, void* stream);
 
+/*
+ * Test hooks for the attention kernels' own abort path (bf16 only). Same
+ * arguments, layout and ownership as fa_fwd / fa_bwd (dtype bf16, no causal
+ * mask), plus:
+ *   skip_tile  the forward's producer skips the load of key tile `skip_tile`
+ *              of every CTA; the backward's producer skips the Q tile of
+ *              query iteration `skip_tile` of every CTA. Neither the copy nor
+ *              its expected-bytes arrival is issued, so no copy is left in
+ *              flight; the consumers' bounded waits on that tile run out.
+ *              Must be in [1, ceil(N / 128) - 1], else FA_ERR_INVALID_ARG.
+ *   limit_ns   every bounded wait of these launches gives up after this many
+ *              nanoseconds (clamped to [1e3, 2e9]).
+ * Each CTA then records FA_ERR_TIMEOUT in the device status word, waits for
+ * the copies and products it issued, frees its tensor memory and exits; the
+ * outputs are undefined. fa_check_device_status reports (and clears) the
+ * timeout, and the context stays usable for ordinary calls. Not for
+ * production use: the pages have no counterpart; this exercises the bounded
+ * waits every kernel here carries.
+ */
+fa_status fa_debug_fwd_skip_load(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                 int B, int H, int N, int d, float scale, int skip_tile,
+                                 long long limit_ns, void* stream);
+fa_status fa_debug_bwd_skip_load(const void* Q, const void* K, const void* V, const void* O,
+                                 const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                 void* workspace, size_t workspace_bytes, int B, int H, int N,
+                                 int d, float scale, int skip_tile, long long limit_ns,
+                                 void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* fa_status_string(fa_status s);
 
