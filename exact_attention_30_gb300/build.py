@@ -27,6 +27,7 @@ SOURCES = [
     ("fa_api.cu", []),
     ("attn_f32.cu", []),
     ("attn_fwd_bf16.cu", []),
+    ("attn_fwd_bf16_q4.cu", []),
     ("attn_bwd_bf16.cu", []),
     ("fa_noalloc.cu", []),
     ("softmax_rows.cu", []),

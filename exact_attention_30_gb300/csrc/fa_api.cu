@@ -234,13 +234,27 @@ unsigned long long clamp_limit(long long limit_ns) {
   return (unsigned long long)limit_ns;
 }
 
+// The bf16 forward at d = 64 runs on the four-query-tile kernel (one CTA per
+// batch*head and 512-row block) when the problem is fixed-length and
+// non-causal, its grid fills at least three quarters of the GPU's resident
+// CTAs (fewer CTAs leave too many SMs idle; the two-tile kernel's grid, twice
+// as large and split at its tail, then finishes first) and N <= 8192 (on
+// longer sequences the two kernels are level). Everything else runs on the
+// two-tile kernel. `slots`: forward CTAs resident at once (the SM count).
+bool fwd_uses_q4(const SeqArgs& sq, int BH, int d, fa_dtype dt, int slots) {
+  if (dt != FA_BF16 || d != 64 || sq.causal || sq.cu_seqlens != nullptr || sq.N > 8192) return false;
+  const long long ctas = (long long)BH * ((sq.N + 511) / 512);
+  return 4 * ctas >= 3ll * slots;
+}
+
 // Tail split of the bf16 forward for this problem on the current device (only
-// fixed-length, non-causal problems are split; the others: one plain plan).
+// fixed-length, non-causal problems of the two-tile kernel are split; the
+// others: one plain plan).
 FwdTailPlan fwd_tail_plan(const SeqArgs& sq, int BH, int d, fa_dtype dt) {
   const long long qblocks = ((long long)sq.N + 255) / 256;
   const long long units = qblocks * BH;
-  (void)d;
-  if (dt != FA_BF16 || sq.causal || sq.cu_seqlens) return FwdTailPlan{(int)units, 0, 1};
+  if (dt != FA_BF16 || sq.causal || sq.cu_seqlens || fwd_uses_q4(sq, BH, d, dt, fwd_slots()))
+    return FwdTailPlan{(int)units, 0, 1};
   return plan_fwd_tail(units, (sq.N + 127) / 128, fwd_slots());
 }
 
@@ -267,8 +281,10 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   if (!get_encode_fn()) return FA_ERR_CUDA;
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_seq_bf16(&a.tmQ, Q, sq, planes, d, 128) || !encode_seq_bf16(&a.tmK, K, sq, planes, d, 128) ||
-      !encode_seq_bf16(&a.tmV, V, sq, planes, d, 128) || !encode_seq_bf16(&a.tmO, O, sq, planes, d, 128))
+  const bool q4 = fwd_uses_q4(sq, BH, d, dt, fwd_slots());
+  const int kv_rows = q4 ? kFwdQ4KeyTile : 128;  // TMA box height of the K/V tiles
+  if (!encode_seq_bf16(&a.tmQ, Q, sq, planes, d, 128) || !encode_seq_bf16(&a.tmK, K, sq, planes, d, kv_rows) ||
+      !encode_seq_bf16(&a.tmV, V, sq, planes, d, kv_rows) || !encode_seq_bf16(&a.tmO, O, sq, planes, d, 128))
     return FA_ERR_CUDA;
   a.O = O;
   a.LSE = LSE;
@@ -294,6 +310,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   a.n_full = plan.n_full;
   a.n_tail = plan.n_tail;
   a.splits = plan.splits;
+  if (q4) return launch_fwd_bf16_q4(a, BH, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   return launch_fwd_bf16(a, BH, d, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -405,7 +422,7 @@ fa_status fa_fwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int re
   FwdTailPlan p{(int)units, 0, 1};
   if (resident_ctas == 0)
     p = fwd_tail_plan(sq, B * H, d, dt);
-  else if (dt == FA_BF16 && !(flags & FA_CAUSAL))
+  else if (dt == FA_BF16 && !(flags & FA_CAUSAL) && !fwd_uses_q4(sq, B * H, d, dt, resident_ctas))
     p = plan_fwd_tail(units, (N + 127) / 128, resident_ctas);
   *n_full = p.n_full;
   *n_tail = p.n_tail;

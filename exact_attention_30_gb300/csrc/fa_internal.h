@@ -73,6 +73,11 @@ struct FwdArgs {
   int debug_skip_kv;
 };
 cudaError_t launch_fwd_bf16(const FwdArgs& a, int BH, int d, cudaStream_t st);
+// The d = 64 forward with four 128-row query tiles per CTA and 64-key K/V
+// tiles (attn_fwd_bf16_q4.cu): fixed-length, non-causal, unsplit problems;
+// tmK / tmV must have 64-row boxes.
+cudaError_t launch_fwd_bf16_q4(const FwdArgs& a, int BH, cudaStream_t st);
+constexpr int kFwdQ4KeyTile = 64;
 
 // The tail split of the bf16 forward for `units` units of n_kv key tiles on
 // a GPU that runs `slots` forward CTAs at once: the units of the last,

@@ -140,7 +140,8 @@ def _tail_makespan(units, slots, n_full, n_tail, splits):
 @pytest.mark.parametrize("B,H,N,d,slots", [
     (2, 16, 4096, 128, 152), (1, 32, 16384, 128, 152), (4, 16, 1024, 64, 152),
     (1, 10, 4096, 128, 152), (1, 10, 4000, 64, 152), (1, 4, 4096, 128, 152),
-    (1, 200, 1024, 128, 152), (1, 200, 256, 128, 152), (3, 7, 777, 64, 148), (1, 1, 1, 128, 152)])
+    (1, 200, 1024, 128, 152), (1, 200, 256, 128, 152), (3, 7, 777, 64, 148), (1, 1, 1, 128, 152),
+    (2, 16, 4096, 64, 152), (1, 16, 16384, 64, 152)])
 def test_forward_tail_split_plan_on_the_host(lib, B, H, N, d, slots):
     """The forward's tail split covers every unit once, splits only the last,
     partly filled wave (never with fewer than four key tiles per range, at
@@ -150,7 +151,11 @@ def test_forward_tail_split_plan_on_the_host(lib, B, H, N, d, slots):
     n_kv = -(-N // 128)
     nf, nt, sp = fa.fa_fwd_plan(B, H, N, d, resident_ctas=slots)
     assert nf + nt == units and sp >= 1 and (sp == 1) == (nt == 0)
-    if sp > 1:
+    # d = 64 problems whose four-tile grid (one CTA per 512 rows) fills at
+    # least 3/4 of the resident CTAs, N <= 8192, run unsplit on that kernel
+    if d == 64 and N <= 8192 and 4 * B * H * -(-N // 512) >= 3 * slots:
+        assert (nf, nt, sp) == (units, 0, 1)
+    elif sp > 1:
         assert nt == units % slots and units >= slots
         assert 2 <= sp <= 4 and n_kv // sp >= 4 and nt * sp <= slots
         assert sp == min(slots // nt, 4, n_kv // 4)
