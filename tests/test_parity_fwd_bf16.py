@@ -115,3 +115,61 @@ def test_outputs_written_everywhere_and_nowhere_else():
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     assert torch.isnan(obuf[:guard]).all() and torch.isnan(obuf[guard + n:]).all()
     assert torch.isnan(lbuf[:guard]).all() and torch.isnan(lbuf[guard + B * H * N:]).all()
+
+
+def _runs_on_four_tile_kernel(B, H, N, d):
+    """The routing rule fa.h states for fa_fwd_plan: bf16, d = 64, non-causal,
+    N <= 8192 and B*H*ceil(N/512) >= 3/4 of the SMs."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return d == 64 and N <= 8192 and 4 * B * H * -(-N // 512) >= 3 * sms
+
+
+@pytest.mark.parametrize("N,H", [(1, 160), (63, 160), (64, 160), (65, 160), (300, 160), (511, 160),
+                                 (512, 160), (513, 80), (1000, 80), (1536, 60), (2049, 40)])
+def test_four_tile_d64_forward_ragged_lengths(N, H):
+    """Ragged lengths on the four-query-tile d = 64 kernel: key tiles of 64
+    with a masked last tile, query tiles past N inside a 512-row block, and
+    rows past N not written."""
+    B, d = 1, 64
+    assert _runs_on_four_tile_kernel(B, H, N, d)
+    q, k, v, _ = random_qkv(B, H, N, d, torch.bfloat16, seed=7000 + N, with_do=False)
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), scale)
+    assert fa.fa_check_device_status() == fa.FA_OK
+    _check_heads(q, k, v, o, lse, scale, [(0, 0), (0, H // 2), (0, H - 1)])
+
+
+def test_four_tile_d64_forward_rescale_and_large_scores():
+    # keys growing along the sequence (the reference max moves on every key
+    # tile, so O is rescaled in TMEM) and scale 1 (scores ~ N(0, 64))
+    B, H, N, d = 1, 128, 1024, 64
+    assert _runs_on_four_tile_kernel(B, H, N, d)
+    q, k, v, _ = random_qkv(B, H, N, d, torch.bfloat16, seed=71, with_do=False)
+    ramp = torch.linspace(0.1, 6.0, N).view(1, 1, N, 1)
+    kr = (k.float().abs() * ramp).to(torch.bfloat16)
+    qr = (q.float().abs() + 0.5).to(torch.bfloat16)
+    o, lse = fa.fa_fwd(qr.cuda(), kr.cuda(), v.cuda(), 0.125)
+    _check_heads(qr, kr, v, o, lse, 0.125, [(0, 0), (0, 127)])
+    o, lse = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), 1.0)
+    assert fa.fa_check_device_status() == fa.FA_OK
+    _check_heads(q, k, v, o, lse, 1.0, [(0, 3), (0, 100)])
+
+
+def test_four_tile_d64_outputs_written_everywhere_and_nowhere_else():
+    B, H, N, d = 1, 120, 700, 64
+    assert _runs_on_four_tile_kernel(B, H, N, d)
+    q, k, v, _ = random_qkv(B, H, N, d, torch.bfloat16, seed=23, with_do=False)
+    n = B * H * N * d
+    guard = 4096
+    obuf = torch.full((n + 2 * guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lbuf = torch.full((B * H * N + 2 * guard,), float("nan"), dtype=torch.float32, device="cuda")
+    o = obuf[guard:guard + n].view(B, H, N, d)
+    lse = lbuf[guard:guard + B * H * N].view(B, H, N)
+    fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), 0.125, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    assert torch.isnan(obuf[:guard]).all() and torch.isnan(obuf[guard + n:]).all()
+    assert torch.isnan(lbuf[:guard]).all() and torch.isnan(lbuf[guard + B * H * N:]).all()
+    # deterministic
+    o2, l2 = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), 0.125)
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
