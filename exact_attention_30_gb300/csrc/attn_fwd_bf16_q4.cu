@@ -28,8 +28,11 @@
 //                P_t(j) V_j then S_t(j+1) = Q_t K_{j+1}^T (P over S: the next
 //                S is ordered after the P V product that reads P).
 //   warps 2-17   softmax, warpgroup g = query tile g, one thread per row.
-// Fixed-length, non-causal problems only (the host routes the others to the
-// two-tile kernel). Every wait is bounded; on expiry the kernel records a
+// Fixed-length problems, causal or not (packed variable-length batches go to
+// the two-tile kernel). Causal attention: query tile t of a 512-row block
+// runs the 64-key tiles up to its diagonal (two tiles more than tile t - 1),
+// the last two of them masked per row; the grid lists the blocks with the
+// most key tiles first. Every wait is bounded; on expiry the kernel records a
 // timeout, drains its copies and products, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -83,6 +86,7 @@ __device__ __forceinline__ void q4_chunk32(const uint32_t (&r)[32], uint32_t (&p
   }
 }
 
+template <bool CAUSAL>
 __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __grid_constant__ FwdArgs a) {
   using C = Q4Cfg;
   extern __shared__ uint8_t smem_raw[];
@@ -99,9 +103,18 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qblocks = (a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT);
-  const int bh = (int)blockIdx.x / qblocks;
-  const int qblk = (int)blockIdx.x - bh * qblocks;
+  constexpr bool causal = CAUSAL;  // a separate instance: the unmasked path stays as lean as before
+  int bh, qblk;
+  if (causal) {
+    // causal grids: (heads of a group, query blocks from the last = most key
+    // tiles to the first, head groups): longest first within a group
+    bh = (int)(blockIdx.z * gridDim.x + blockIdx.x);
+    qblk = (int)(gridDim.y - 1 - blockIdx.y);
+  } else {
+    const int qblocks = (a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT);
+    bh = (int)blockIdx.x / qblocks;
+    qblk = (int)blockIdx.x - bh * qblocks;
+  }
   if (bh >= a.BH) return;
   const int N = a.seq.N;
   const int q0 = qblk * (C::BM * C::QT);
@@ -109,6 +122,10 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
   const int plane = bh;
   // query tiles with at least one row inside the sequence
   const int n_tiles = min(C::QT, (N - q0 + C::BM - 1) / C::BM);
+  // key tiles of query tile t: all of them, or (causal) those up to its
+  // diagonal, which ends at key q0 + 128 (t + 1) - 1
+  auto n_own = [&](int t) { return causal ? min(n_kv, (q0 + C::BM * (t + 1)) / C::BN) : n_kv; };
+  const int n_max = n_own(n_tiles - 1);  // the last live tile sees the most keys
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < C::QT; ++t) mbar_init(BAR(B_QFULL + t), 1);
@@ -149,7 +166,7 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
       int last_k[C::STAGES], last_v[C::STAGES];  // last tile loaded into each slot
 #pragma unroll
       for (int s = 0; s < C::STAGES; ++s) last_k[s] = last_v[s] = -1;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < n_max; ++j) {
         if (*abort_flag) break;
         const int s = j % C::STAGES;
         const uint32_t ph = (j / C::STAGES) & 1;
@@ -213,20 +230,22 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
       mma_commit(BAR(B_SFULL + t), leader);
     }
     if (ok) mma_commit(BAR(B_KEMPTY + 0), leader);
-    for (int j = 0; ok && j < n_kv; ++j) {
+    for (int j = 0; ok && j < n_max; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       const int s = j % C::STAGES, s1 = (j + 1) % C::STAGES;
       const uint32_t ph = (j / C::STAGES) & 1, ph1 = ((j + 1) / C::STAGES) & 1;
-      const bool more = j + 1 < n_kv;
+      const bool more = j + 1 < n_max;
       if (!wait(B_VFULL + s, ph)) { ok = false; break; }
       if (more && !wait(B_KFULL + s1, ph1)) { ok = false; break; }
       for (int t = 0; t < n_tiles; ++t) {
+        const int nt = n_own(t);
+        if (j >= nt) continue;  // (causal) this query tile is past its diagonal
         // P_t(j) V_j, then S_t(j+1) over the columns P_t(j) occupies
         if (!wait(B_PFULL + t, j & 1)) { ok = false; break; }
         tc_fence_after();
         issue_pv(t, s, j > 0);
         mma_commit(BAR(B_ODONE + t), leader);
-        if (more) {
+        if (j + 1 < nt) {
           issue_s(t, s1);
           mma_commit(BAR(B_SFULL + t), leader);
         }
@@ -250,15 +269,18 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
     const uint32_t s_addr = lane_addr + C::S_COL(t);
     const uint32_t o_addr = lane_addr + C::O_COL(t);
     const uint64_t c22 = f2_pack(a.scale_log2, a.scale_log2);
+    const int nt = live_tile ? n_own(t) : 0;
+    const int key_end = causal ? min(N, row + 1) : N;  // keys this row sees: [0, key_end)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; live_tile && j < n_kv; ++j) {
+    for (int j = 0; j < nt; ++j) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
       const bool w = mbar_wait(BAR(B_SFULL + t), j & 1, a.status, a.wait_limit_ns);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
-      // Only the sequence's last key tile can hold keys past N.
-      const int valid = N - j * C::BN;
+      // Keys past N (the sequence's last key tile) and, causal, keys after
+      // this row (the last two key tiles of the query tile) are masked.
+      const int valid = key_end - j * C::BN;
       const bool mask = valid < C::BN;
       // Both 32-column halves of the row are loaded at once (one TMEM round
       // trip); the row max comes first, so every exponential is computed
@@ -325,7 +347,7 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
     }
     tmem_st_wait();  // no TMEM store may be in flight when the loop is left early
     if (ok && live_tile) {
-      const bool w = mbar_wait(BAR(B_ODONE + t), (n_kv - 1) & 1, a.status, a.wait_limit_ns);
+      const bool w = mbar_wait(BAR(B_ODONE + t), (nt - 1) & 1, a.status, a.wait_limit_ns);
       ok = __all_sync(0xffffffffu, w);
     }
     // the tile's four warps take one decision (they share the store barrier)
@@ -383,12 +405,18 @@ __global__ void __launch_bounds__(Q4Cfg::THREADS, 1) fwd_bf16_q4_kernel(const __
 
 cudaError_t launch_fwd_bf16_q4(const FwdArgs& a, int BH, cudaStream_t st) {
   using C = Q4Cfg;
-  if (a.seq.causal || a.seq.cu_seqlens || a.splits != 1) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_ALLOC);
+  if (a.seq.cu_seqlens || a.splits != 1) return cudaErrorInvalidValue;
+  auto kernel = a.seq.causal ? fwd_bf16_q4_kernel<true> : fwd_bf16_q4_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const long long qblocks = ((long long)a.seq.N + C::BM * C::QT - 1) / (C::BM * C::QT);
-  fwd_bf16_q4_kernel<<<(unsigned)(qblocks * BH), C::THREADS, C::SMEM_ALLOC, st>>>(a);
+  dim3 grid((unsigned)(qblocks * BH));
+  if (a.seq.causal) {
+    // every CTA of a head streams the head's K and V (budget: most of L2)
+    const int hpg = causal_heads_per_group(BH, 4ll * a.seq.N * C::D, 96ll << 20);
+    grid = dim3((unsigned)hpg, (unsigned)qblocks, (unsigned)((BH + hpg - 1) / hpg));
+  }
+  kernel<<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
   return cudaGetLastError();
 }
 

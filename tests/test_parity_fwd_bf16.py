@@ -118,7 +118,7 @@ def test_outputs_written_everywhere_and_nowhere_else():
 
 
 def _runs_on_four_tile_kernel(B, H, N, d):
-    """The routing rule fa.h states for fa_fwd_plan: bf16, d = 64, non-causal,
+    """The routing rule fa.h states for fa_fwd_plan: bf16, d = 64, causal or not,
     N <= 8192 and B*H*ceil(N/512) >= 3/4 of the SMs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     return d == 64 and N <= 8192 and 4 * B * H * -(-N // 512) >= 3 * sms
@@ -173,3 +173,22 @@ def test_four_tile_d64_outputs_written_everywhere_and_nowhere_else():
     # deterministic
     o2, l2 = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), 0.125)
     assert torch.equal(o, o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("N,H", [(1, 160), (100, 160), (512, 160), (513, 80), (1000, 80), (2048, 40)])
+def test_four_tile_d64_causal_forward(N, H):
+    """Causal attention on the four-query-tile d = 64 kernel: each query tile
+    stops at its diagonal, the last two 64-key tiles masked per row, blocks
+    scheduled longest first."""
+    B, d = 1, 64
+    assert _runs_on_four_tile_kernel(B, H, N, d)
+    q, k, v, _ = random_qkv(B, H, N, d, torch.bfloat16, seed=9000 + N, with_do=False)
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), scale, causal=True)
+    assert fa.fa_check_device_status() == fa.FA_OK
+    q64, k64, v64 = to64(q), to64(k), to64(v)
+    o64, l64 = to64(o), to64(lse)
+    for h in (0, H // 2, H - 1):
+        O, LSE = attention_fwd(q64[0, h], k64[0, h], v64[0, h], scale, causal=True)
+        assert rel_max(o64[0, h], O) <= TOL_BF16_O, h
+        assert max_abs(l64[0, h], LSE) <= TOL_BF16_LSE, h
