@@ -124,7 +124,7 @@ def read_peaks():
 
 # A timed region counts as "sustained" (the power-capped GEMM loop's figure)
 # only when it lasted at least this long and the clock sampler saw the power
-# cap active; anything shorter is a burst, judged against the burst GEMM.
+# cap active; anything shorter is a burst, compared with the burst GEMM.
 SUSTAINED_MIN_SECONDS = 2.0
 
 
