@@ -24,7 +24,7 @@ import re
 import torch
 
 __all__ = [
-    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_fwd_varlen", "fa_bwd_varlen",
+    "fa_fwd", "fa_bwd", "fa_bwd_stage", "fa_bwd_plan", "fa_fwd_varlen", "fa_bwd_varlen",
     "fa_bwd_varlen_workspace_bytes", "FA_CAUSAL", "fa_bwd_workspace_bytes", "fa_softmax_rows", "fa_decode",
     "fa_decode_workspace_bytes", "fa_decode_plan", "fa_check_device_status",
     "fa_debug_timeout_probe", "fa_status_string", "fa_version", "library_path", "load_library",
@@ -54,6 +54,7 @@ _SIGNATURES = {
     "fa_bwd_varlen_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
     "fa_bwd_varlen": (_ci, [_vp] * 11 + [_sz, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _ci, _vp]),
     "fa_bwd_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
+    "fa_bwd_plan": (_ci, [_ci] * 7 + [ctypes.POINTER(_ci)] * 3),
     "fa_bwd": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_stage": (_ci, [_ci] + [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _vp]),
     "fa_bwd_noalloc": (_ci, [_vp] * 9 + [_ci, _ci, _ci, _ci, _cf, _ci, _vp]),
@@ -158,6 +159,17 @@ def fa_fwd_plan(B: int, H: int, N: int, d: int, causal: bool = False, dtype=torc
     rc = load_library().fa_fwd_plan(B, H, N, d, FA_CAUSAL if causal else 0, code, resident_ctas,
                                     ctypes.byref(nf), ctypes.byref(nt), ctypes.byref(sp))
     _raise(rc, "fa_fwd_plan")
+    return nf.value, nt.value, sp.value
+
+
+def fa_bwd_plan(B: int, H: int, N: int, d: int, causal: bool = False, dtype=torch.bfloat16,
+                resident_ctas: int = 0):
+    """(n_full, n_tail, splits) of the backward main kernel's schedule (fa_bwd_plan in fa.h)."""
+    nf, nt, sp = _ci(), _ci(), _ci()
+    code = FA_BF16 if dtype == torch.bfloat16 else FA_F32
+    rc = load_library().fa_bwd_plan(B, H, N, d, FA_CAUSAL if causal else 0, code, resident_ctas,
+                                    ctypes.byref(nf), ctypes.byref(nt), ctypes.byref(sp))
+    _raise(rc, "fa_bwd_plan")
     return nf.value, nt.value, sp.value
 
 

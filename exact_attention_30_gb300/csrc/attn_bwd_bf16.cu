@@ -108,7 +108,16 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 // 3. dQ convert
 // ----------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a) {
+__device__ void bwd_tail_merge_rows(const BwdArgs& a, long long w);
+
+// Blocks past the conversion's own (`conv_blocks`) add up the partial dK and
+// dV of the split units (bwd_tail_merge_rows), in the same launch.
+template <int D>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a, unsigned conv_blocks) {
+  if (blockIdx.x >= conv_blocks) {
+    bwd_tail_merge_rows<D>(a, ((long long)(blockIdx.x - conv_blocks) * blockDim.x + threadIdx.x) >> 5);
+    return;
+  }
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 elements
   const long long groups = (long long)a.planes * a.seq.total * (D / 8);
   if (idx >= groups) return;
@@ -125,6 +134,41 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const BwdArgs a) {
   u.w = pack_bf16x2(f * y.z, f * y.w);
   *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dQ) + (size_t)plane * (size_t)a.seq.plane_stride +
                              (size_t)n * (size_t)a.seq.row_stride + g * 8) = u;
+}
+
+// The query ranges of a split unit summed ("Lesson 1" §5: dK_j and dV_j are
+// sums over the query tiles), dK times the softmax scale, to bf16. One warp
+// per key row w = tail unit * 128 + row of a split unit, lanes along d.
+template <int D>
+__device__ void bwd_tail_merge_rows(const BwdArgs& a, long long w) {
+  constexpr int PER = D / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)a.n_tail * 128) return;
+  const int tu = (int)(w >> 7), r = (int)(w & 127);
+  const int kblocks = (a.seq.N + 127) / 128;
+  const int u = a.n_full + tu;
+  const int bh = u / kblocks, kb = u - bh * kblocks;
+  const int key = kb * 128 + r;
+  if (key >= a.seq.N) return;
+  float sv[PER], sk[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) sv[e] = sk[e] = 0.f;
+  for (int p = 0; p < a.splits; ++p) {
+    const float* base = a.dKVpart + ((size_t)(tu * a.splits + p) * 2) * 128 * D + (size_t)r * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      sv[e] += base[e];
+      sk[e] += base[(size_t)128 * D + e];
+    }
+  }
+  const size_t off = (size_t)bh * (size_t)a.seq.plane_stride + (size_t)key * (size_t)a.seq.row_stride + lane * PER;
+  __nv_bfloat16* dv = reinterpret_cast<__nv_bfloat16*>(a.dV) + off;
+  __nv_bfloat16* dk = reinterpret_cast<__nv_bfloat16*>(a.dK) + off;
+#pragma unroll
+  for (int e = 0; e < PER; e += 2) {
+    *reinterpret_cast<uint32_t*>(dv + e) = pack_bf16x2(sv[e], sv[e + 1]);
+    *reinterpret_cast<uint32_t*>(dk + e) = pack_bf16x2(a.scale * sk[e], a.scale * sk[e + 1]);
+  }
 }
 
 // ----------------------------------------------------------------------------
@@ -215,18 +259,43 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
-  // causal grids: (heads of a group, key tiles in increasing order = most
-  // query tiles first, head groups)
-  const int bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
-  const int kb = causal ? (int)blockIdx.y : (int)blockIdx.x;
+  int bh, kb;
+  int tail_unit = -1, part = 0;  // split units: index among them, query range
+  if (a.splits > 1) {
+    // tail-split grid (fixed length, non-causal): one CTA per unit
+    // (batch*head, key tile), key tile fastest; the units from n_full on
+    // run as a.splits query ranges, one CTA each
+    const int kblocks = (a.seq.N + C::BK - 1) / C::BK;
+    int u = (int)blockIdx.x;
+    if (u >= a.n_full) {
+      const int r = u - a.n_full;
+      tail_unit = r / a.splits;
+      part = r - tail_unit * a.splits;
+      u = a.n_full + tail_unit;
+    }
+    bh = u / kblocks;
+    kb = u - bh * kblocks;
+  } else {
+    // causal grids: (heads of a group, key tiles in increasing order = most
+    // query tiles first, head groups)
+    bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
+    kb = causal ? (int)blockIdx.y : (int)blockIdx.x;
+  }
   if (bh >= a.BH) return;  // past the last head of the last group
   const SeqView sv = seq_view(a.seq, bh, a.status);
   const int N = sv.len;  // queries = keys of this sequence
   const int k0 = kb * C::BK;
   if (k0 >= N) return;  // the whole CTA: no key of this sequence here
   const int n_q = (N + C::BQ - 1) / C::BQ;
-  const int i_begin = causal ? kb : 0;  // query tiles before the diagonal see no key of this tile
-  const int n_it = n_q - i_begin;       // >= 1
+  // query tiles i_begin .. i_end-1: all of them, those at or after the
+  // diagonal (causal: the earlier ones see no key of this tile), or this
+  // CTA's range of a split unit
+  int i_begin = causal ? kb : 0, i_end = n_q;
+  if (tail_unit >= 0) {
+    i_begin = (int)((long long)part * n_q / a.splits);
+    i_end = (int)((long long)(part + 1) * n_q / a.splits);
+  }
+  const int n_it = i_end - i_begin;  // >= 1
   const int y0 = sv.start, plane = sv.plane;
   const size_t ws_row0 = (size_t)plane * a.ws_rows + (size_t)y0;  // workspace row of query 0
 
@@ -586,8 +655,26 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       *abort_flag = 1;
     } else {
       // epilogue: group 0 writes dV, group 1 writes dK (which carries the
-      // softmax scale of dS)
+      // softmax scale of dS); a query range of a split unit leaves its fp32
+      // partial sums (dK unscaled) for the dQ-convert stage to add up
       tc_fence_after();
+      if (tail_unit >= 0) {
+        float* prow = a.dKVpart + ((size_t)(tail_unit * a.splits + part) * 2 + g) * (size_t)C::BK * D +
+                      (size_t)r * D;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          tmem_ld32(lane_addr + (g == 0 ? C::COL_DV : C::COL_DK) + 32 * q, v);
+          tmem_ld_wait();
+          if (key_live) {
+            float4* d4 = reinterpret_cast<float4*>(prow + 32 * q);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                  __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          }
+        }
+      } else {
       const size_t out_row = key_live ? seq_row_offset(a.seq, sv, k0 + r) : 0;
       const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
       const float f = g == 0 ? 1.f : scale;
@@ -607,11 +694,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
         }
       }
+      }
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ reduction
-    const int wq = warp & 3;
-    const int t = wq * 32 + lane;  // TMEM lane: d index (dQ^T) or query row (dQ)
+    const int wq = warp & 3;  // TMEM lanes 32wq..32wq+31: d indices (dQ^T) or query rows (dQ)
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     constexpr int NCOL = C::DQ_T ? C::BQ : D;  // columns of the dQ tile
     constexpr int HALF = NCOL / 2;             // read in two halves (register budget)
@@ -716,7 +803,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
     if (e != cudaSuccess) return e;
     const unsigned kblocks = (unsigned)((a.seq.N + C::BK - 1) / C::BK);
     dim3 grid(kblocks, (unsigned)BH);
-    if (a.seq.causal) {
+    if (a.splits > 1) {
+      if (a.seq.causal || a.seq.cu_seqlens || a.dKVpart == nullptr || a.n_tail < 1 ||
+          (long long)a.n_full + a.n_tail != (long long)kblocks * BH)
+        return cudaErrorInvalidValue;
+      grid = dim3((unsigned)((long long)a.n_full + (long long)a.n_tail * a.splits));
+    } else if (a.seq.causal) {
       // every CTA of a head streams the head's Q and dO and adds into its dQ accumulator
       const int hpg = causal_heads_per_group(BH, 8ll * a.seq.N * D, 48ll << 20);
       grid = dim3((unsigned)hpg, kblocks, (unsigned)((BH + hpg - 1) / hpg));
@@ -727,13 +819,36 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
   }
   if (stages & kStageConvert) {
     const long long groups = (long long)a.planes * a.seq.total * (D / 8);
-    dq_convert_kernel<D><<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(a);
+    const unsigned conv_blocks = (unsigned)((groups + 255) / 256);
+    // plus one warp per key row of a split unit (8 rows per block)
+    const unsigned merge_blocks = a.splits > 1 ? (unsigned)(((long long)a.n_tail * 128 + 7) / 8) : 0u;
+    dq_convert_kernel<D><<<conv_blocks + merge_blocks, 256, 0, st>>>(a, conv_blocks);
     e = cudaGetLastError();
   }
   return e;
 }
 
 }  // namespace
+
+BwdTailPlan plan_bwd_tail(long long units, int n_q, int slots) {
+  BwdTailPlan p{(int)units, 0, 1};
+  if (units < 1 || slots < 1 || n_q < 1) return p;
+  const long long rem = units % slots;
+  if (units < slots || rem == 0) return p;  // no whole wave before the tail, or no tail
+  long long sp = slots / rem;
+  if (sp > 4) sp = 4;
+  if (sp > n_q / 4) sp = n_q / 4;
+  if (sp < 2) return p;
+  p.n_full = (int)(units - rem);
+  p.n_tail = (int)rem;
+  p.splits = (int)sp;
+  return p;
+}
+
+size_t bwd_tail_part_bytes(const BwdTailPlan& p, int d) {
+  if (p.splits <= 1 || p.n_tail <= 0) return 0;
+  return ((size_t)p.n_tail * p.splits * 2 * 128 * d * 4 + 255) & ~(size_t)255;
+}
 
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st) {
   if (d == 128) return launch_bwd_d<128>(a, BH, stages, st);

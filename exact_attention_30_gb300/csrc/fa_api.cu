@@ -157,13 +157,17 @@ SeqArgs varlen_seq(const int* cu_seqlens, int H, int total, int max_seqlen, int 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdWorkspaceLayout {
-  size_t dqacc, lse2, drow, total;
+  size_t dqacc, lse2, drow, part, total;
   int planes, ws_rows;
+  BwdTailPlan plan;
 };
 // fp32: D per row ([planes, total]). bf16: fp32 dQ accumulator
-// [planes, ws_rows, d] and two per-row statistics [planes, ws_rows].
+// [planes, ws_rows, d], two per-row statistics [planes, ws_rows] and, when the
+// schedule splits its tail (fixed length, non-causal, on the current device),
+// the split units' fp32 partial dV and dK.
 BwdWorkspaceLayout bwd_layout(const SeqArgs& sq, int B, int d, fa_dtype dt) {
   BwdWorkspaceLayout L{};
+  L.plan = BwdTailPlan{0, 0, 1};
   L.planes = sq.cu_seqlens ? sq.H : B * sq.H;
   const size_t P = (size_t)L.planes;
   if (dt == FA_F32) {
@@ -176,7 +180,10 @@ BwdWorkspaceLayout bwd_layout(const SeqArgs& sq, int B, int d, fa_dtype dt) {
   L.dqacc = 0;
   L.lse2 = align_up(P * L.ws_rows * d * sizeof(float), 256);
   L.drow = L.lse2 + align_up(P * L.ws_rows * sizeof(float), 256);
-  L.total = L.drow + align_up(P * L.ws_rows * sizeof(float), 256);
+  L.part = L.drow + align_up(P * L.ws_rows * sizeof(float), 256);
+  if (!sq.causal && sq.cu_seqlens == nullptr)
+    L.plan = plan_bwd_tail((long long)B * sq.H * ((sq.N + 127) / 128), (sq.N + 127) / 128, fwd_slots());
+  L.total = L.part + bwd_tail_part_bytes(L.plan, d);
   return L;
 }
 
@@ -372,6 +379,10 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.status = status;
   a.wait_limit_ns = wait_limit_ns;
   a.debug_skip_q = debug_skip;
+  a.n_full = L.plan.n_full;
+  a.n_tail = L.plan.n_tail;
+  a.splits = L.plan.splits;
+  a.dKVpart = L.plan.splits > 1 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
   return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -453,6 +464,26 @@ fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, fl
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt) {
   if (check_shape(B, H, N, d, 1.0f, dt) != FA_OK) return 0;
   return bwd_layout(fixed_seq(H, N, d, false), B, d, dt).total;
+}
+
+fa_status fa_bwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int resident_ctas,
+                      int* n_full, int* n_tail, int* splits) {
+  if (!n_full || !n_tail || !splits || resident_ctas < 0) return FA_ERR_INVALID_ARG;
+  const fa_status s = check_shape(B, H, N, d, 1.f, dt);
+  if (s != FA_OK) return s;
+  if (flags & ~FA_CAUSAL) return FA_ERR_INVALID_ARG;
+  const long long units = (long long)B * H * ((N + 127) / 128);
+  BwdTailPlan p{(int)units, 0, 1};
+  if (dt == FA_BF16 && !(flags & FA_CAUSAL)) {
+    if (resident_ctas == 0)
+      p = bwd_layout(fixed_seq(H, N, d, false), B, d, dt).plan;
+    else
+      p = plan_bwd_tail(units, (N + 127) / 128, resident_ctas);
+  }
+  *n_full = p.n_full;
+  *n_tail = p.n_tail;
+  *splits = p.splits;
+  return FA_OK;
 }
 
 size_t fa_bwd_varlen_workspace_bytes(int B, int H, int total, int max_seqlen, int d, fa_dtype dt) {

@@ -117,8 +117,25 @@ struct BwdArgs {
   // nor the expected-bytes arrival of the Q tile of this iteration, so the
   // consumers' bounded waits run out. -1: load everything.
   int debug_skip_q;
+  // Tail split (fixed length, non-causal, splits > 1): units (batch*head,
+  // 128-key tile), key tile fastest, 0..n_full-1 run whole; the n_tail units
+  // after them run as `splits` ranges of query tiles each, one CTA per range,
+  // leaving fp32 partial dV and dK (unscaled) in dKVpart; the dQ-convert
+  // stage adds the ranges up. splits = 1: the usual 2-D grids.
+  int n_full, n_tail, splits;
+  float* dKVpart;  // fp32 [n_tail][splits][2 (dV, dK)][128][d]
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
+// The backward's tail split for `units` (batch*head, key tile) units with n_q
+// query tiles each on a GPU running `slots` backward CTAs at once (one per
+// SM): the units of a last wave that fills at most half the GPU run as
+// splits = min(slots / (units mod slots), 4, n_q / 4) >= 2 query ranges.
+struct BwdTailPlan {
+  int n_full, n_tail, splits;
+};
+BwdTailPlan plan_bwd_tail(long long units, int n_q, int slots);
+// fp32 partial dV/dK bytes of a plan (0 when nothing is split).
+size_t bwd_tail_part_bytes(const BwdTailPlan& p, int d);
 // Row padding used by the bf16 backward workspace: ws_rows = roundup(total, 128)
 // (+128 with variable lengths, where a sequence's last tile may start anywhere).
 constexpr int kBwdRowPad = 128;

@@ -157,6 +157,23 @@ fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, fl
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt);
 
 /*
+ * The schedule of the bf16 backward's main kernel for this problem (no GPU
+ * work). It runs one CTA per (batch*head, 128-key tile) unit, one CTA per SM;
+ * when the last wave fills at most half of the SMs, its *n_tail units run as
+ * *splits ranges of query tiles each, one CTA per range, and the dQ-convert
+ * stage adds their partial dK and dV up ("Lesson 1: FlashAttention core
+ * idea" §5: dK_j and dV_j are sums over the query tiles). *n_full units run
+ * whole (*splits = 1, *n_tail = 0: nothing split). The rule, with W CTAs at
+ * once and U units: splits = min(W / (U mod W), 4, query tiles / 4) when that
+ * is at least 2 and U >= W; bf16, fixed length, non-causal only. The partial
+ * sums are part of fa_bwd_workspace_bytes().
+ *   resident_ctas : W; 0 plans for the current device.
+ * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (as fa_bwd_ex).
+ */
+fa_status fa_bwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int resident_ctas,
+                      int* n_full, int* n_tail, int* splits);
+
+/*
  * Backward pass with recomputation.  "Lesson 1" §5: with P rebuilt from the
  * saved statistics, dV = P^T dO, dP = dO V^T,
  * dS = P o (dP - rowsum(dO o O)) * scale, dQ = dS K, dK = dS^T Q.

@@ -213,3 +213,33 @@ def test_python_binding_checks_varlen_arguments():
     cu = torch.tensor([0, 10], dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA"):
         fa.fa_fwd_varlen(q, q, q, cu, 10)
+
+
+@pytest.mark.parametrize("B,H,N,d,slots", [
+    (2, 16, 4096, 128, 152), (4, 16, 1024, 64, 152), (1, 16, 4096, 128, 152), (1, 10, 2000, 128, 152),
+    (1, 32, 16384, 128, 152), (1, 1, 1, 64, 152), (1, 5, 8192, 64, 148), (3, 7, 700, 128, 152)])
+def test_backward_tail_split_plan_on_the_host(lib, B, H, N, d, slots):
+    """The backward's tail split covers every (head, key tile) unit once, splits
+    only a last wave that fills at most half the SMs (ranges of at least four
+    query tiles, at most four ranges, all in that wave) and shortens the
+    schedule; causal and fp32 problems are never split."""
+    n_q = -(-N // 128)
+    units = B * H * n_q
+    nf, nt, sp = fa.fa_bwd_plan(B, H, N, d, resident_ctas=slots)
+    assert nf + nt == units and sp >= 1 and (sp == 1) == (nt == 0)
+    if sp > 1:
+        assert nt == units % slots and units >= slots
+        assert 2 <= sp <= 4 and n_q // sp >= 4 and nt * sp <= slots
+        assert sp == min(slots // nt, 4, n_q // 4)
+        assert nf // slots + 1.0 / sp < -(-units // slots)
+    else:
+        rem = units % slots
+        assert rem == 0 or units < slots or min(slots // rem, 4, n_q // 4) < 2
+    assert fa.fa_bwd_plan(B, H, N, d, causal=True, resident_ctas=slots) == (units, 0, 1)
+    assert fa.fa_bwd_plan(B, H, N, d, dtype=torch.float32, resident_ctas=slots) == (units, 0, 1)
+
+
+def test_backward_plan_without_a_gpu_splits_nothing(lib):
+    # no device: the current-device plan splits nothing and asks for no partials
+    B, H, N, d = 4, 16, 1024, 64
+    assert fa.fa_bwd_plan(B, H, N, d) == (B * H * (N // 128), 0, 1)
