@@ -149,10 +149,11 @@ fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, fl
                         float scale, int flags, fa_dtype dt, void* stream);
 
 /*
- * Bytes of device scratch that fa_bwd needs for this problem (0 on invalid
- * arguments). The caller allocates it; its contents on entry do not matter.
- * Holds the fp32 dQ accumulator and per-row statistics derived from
- * D = rowsum(dO o O) and the LSE.
+ * Bytes of device scratch that fa_bwd needs for this problem on the CURRENT
+ * device (0 on invalid arguments). The caller allocates it; its contents on
+ * entry do not matter. Holds the fp32 dQ accumulator, per-row statistics
+ * derived from D = rowsum(dO o O) and the LSE and, when the schedule splits
+ * its tail (fa_bwd_plan), the split units' fp32 partial dK and dV.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt);
 
@@ -196,11 +197,15 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  *   FA_BWD_PREPROCESS (0): per-row statistics from D = rowsum(dO o O) and
  *                          the LSE into the workspace; zero the workspace's
  *                          dQ accumulator.
- *   FA_BWD_MAIN       (1): recompute P tile by tile; write dK, dV; add dQ
- *                          into the workspace accumulator (for bf16 without
- *                          the softmax scale). Needs stage 0 done.
+ *   FA_BWD_MAIN       (1): recompute P tile by tile; write dK, dV (the
+ *                          split units of fa_bwd_plan: partial sums into the
+ *                          workspace); add dQ into the workspace accumulator
+ *                          (for bf16 without the softmax scale). Needs stage
+ *                          0 done.
  *   FA_BWD_DQ_CONVERT (2): workspace dQ accumulator -> dQ in dtype `dt`
- *                          (bf16: the scale is applied here). Needs stage 1.
+ *                          (bf16: the scale is applied here), and the split
+ *                          units' partial dK, dV added up into dK, dV.
+ *                          Needs stage 1.
  * Stages run in that order on one workspace; fa_bwd == stages 0, 1, 2.
  * Errors: as fa_bwd, plus FA_ERR_INVALID_ARG for an unknown stage.
  */
