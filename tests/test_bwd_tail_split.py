@@ -70,3 +70,25 @@ def test_split_backward_is_repeatable_and_stagewise_equal():
     # dQ is added by the TMA engine in whatever order the CTAs arrive
     for x in (g2[0], outs[0]):
         assert (x.float() - g1[0].float()).abs().max() <= 1e-2 * g1[0].float().abs().max()
+
+
+@pytest.mark.parametrize("B,H,N,d", [(8, 50, 1024, 64), (3, 60, 1536, 128)])
+def test_split_backward_many_heads(B, H, N, d):
+    """Many heads of short sequences (a 2-D grid's worth of units in the split
+    schedule's 1-D grid); sampled heads against the oracle, split ones included."""
+    n_full, n_tail, splits = fa.fa_bwd_plan(B, H, N, d)
+    q, k, v, do = random_qkv(B, H, N, d, torch.bfloat16, seed=B * H + N)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(qc, kc, vc, scale)
+    grads = fa.fa_bwd(qc, kc, vc, o, doc, lse, scale)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    kblocks = -(-N // 128)
+    heads = {0, B * H - 1, (n_full // kblocks) if splits > 1 else B * H // 2}
+    q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
+    for bh in sorted(heads):
+        b, h = divmod(bh, H)
+        ref = attention_bwd(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale)
+        for name, got, r in zip(("dQ", "dK", "dV"), grads, ref):
+            assert rel_max(to64(got[b, h]), r) <= 5e-2, (name, b, h)
