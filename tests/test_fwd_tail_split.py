@@ -9,7 +9,8 @@ sums. Checks, through the C ABI:
   * the split schedule against the plain one (fa_fwd_ex, no scratch) on the
     whole output;
   * a second call on the same scratch gives the same bits (the scratch
-    carries nothing from one call to the next);
+    carries nothing from one call to the next), whatever the scratch held
+    before, and every row is written;
   * a scratch that is too small is refused before launch.
 """
 import math
@@ -101,6 +102,36 @@ def test_split_tail_repeats_bit_for_bit_on_the_same_scratch():
     # the Python entry point takes the same schedule
     o3, l3 = fa.fa_fwd(qc, kc, vc, 0.1)
     assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+@pytest.mark.parametrize("B,H,N,d", [(1, 10, 4096, 128), (1, 2, 20000, 64)])
+def test_split_tail_is_deterministic_for_any_scratch(B, H, N, d):
+    """Twenty calls on scratch filled with 0x00, 0xFF, 0x7F bytes and then on
+    the previous call's leftovers: O starts as NaN each time and comes out
+    with the same bits as the first call."""
+    if fa.fa_fwd_plan(B, H, N, d)[2] == 1:
+        pytest.skip("this GPU's schedule splits nothing for this shape")
+    q, k, v, _ = random_qkv(B, H, N, d, torch.bfloat16, seed=11 + d, with_do=False)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    scale = 1 / math.sqrt(d)
+    nbytes = fa.fa_fwd_workspace_bytes(B, H, N, d)
+    ref = None
+    for i in range(20):
+        ws = torch.full((nbytes,), (0x00, 0xFF, 0x7F)[i % 3], dtype=torch.uint8, device="cuda") if i < 3 else ws
+        o = torch.full_like(qc, float("nan"))
+        lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+        lib = fa.load_library()
+        rc = lib.fa_fwd_ws(qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           ws.data_ptr(), ws.numel(), B, H, N, d, scale, 0, fa.FA_BF16,
+                           torch.cuda.current_stream().cuda_stream)
+        assert rc == fa.FA_OK
+        torch.cuda.synchronize()
+        assert fa.fa_check_device_status() == fa.FA_OK
+        assert not torch.isnan(o).any() and not torch.isnan(lse).any(), i
+        if ref is None:
+            ref = (o, lse)
+        else:
+            assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1]), i
 
 
 def test_split_tail_refuses_a_small_scratch():
