@@ -137,12 +137,11 @@ def bf16_peak(peaks, src, clocks, timed_seconds):
     return peaks["bf16_tflops"], f"{src} bf16 burst ({why})"
 
 
-def fwd_kernel_name(B, H, N, D, dev):
-    """The forward kernel a bf16 fixed-length problem runs on, by the routing
-    rule fa.h documents for fa_fwd_plan: d = 64, N <= 8192 and
-    B*H*ceil(N/512) >= 3/4 of the SMs take the four-query-tile kernel."""
-    import torch
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+def fwd_kernel_name(B, H, N, D, sms):
+    """The forward kernel a bf16 fixed-length problem runs on, on a GPU with
+    `sms` SMs, by the routing rule fa.h documents for fa_fwd_plan: d = 64,
+    N <= 8192 and B*H*ceil(N/512) >= 3/4 of the SMs take the four-query-tile
+    kernel."""
     if D == 64 and N <= 8192 and 4 * B * H * (-(-N // 512)) >= 3 * sms:
         return "fwd_bf16_q4_kernel"
     return f"fwd_bf16_kernel<{D}>"
@@ -541,7 +540,7 @@ def run_gpu(args):
                      "timed_region_s": wall,
                      "algorithmic_flops_per_launch": BWD_FLOPS},
         "components": {
-            "fwd": {"kernel": fwd_kernel_name(B, H, N, D, dev) + (" + fwd_tail_merge_kernel" if fws_bytes else ""),
+            "fwd": {"kernel": fwd_kernel_name(B, H, N, D, torch.cuda.get_device_properties(dev).multi_processor_count) + (" + fwd_tail_merge_kernel" if fws_bytes else ""),
                     "ms": fwd_avg,
                     "tflops": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12,
                     "frac_of_peak": FWD_FLOPS / (fwd_avg * 1e-3) / 1e12 / peak,
