@@ -303,6 +303,33 @@ def cpu_baseline(seconds: float):
                       f"(input generation included)"}
 
 
+def parity_sample(q_h, k_h, v_h, do_h, o, lse, dq, scale):
+    """Part of the CPU-baseline leg: the fp64 oracle on sampled query rows of
+    the bench's own inputs, against the GPU's O, LSE and dQ of the timed step
+    (dQ rows are row-local, so a strip of rows is exact; dK and dV, sums over
+    every query, are left to the parity tests). Errors: max |gpu - ref| /
+    max |ref| over the checked rows for O and dQ, max |gpu - ref| for LSE."""
+    import numpy as np
+
+    from oracle import attention_bwd, attention_fwd_rows
+    rows = sorted(set(np.linspace(0, N - 1, 33).astype(int).tolist()))
+    heads = [(0, 0), (B - 1, H - 1)]
+    err = {"O": 0.0, "LSE": 0.0, "dQ": 0.0}
+    o_h, l_h, dq_h = o.float().cpu(), lse.cpu(), dq.float().cpu()
+    for b, h in heads:
+        f = lambda t: t[b, h].double().numpy()
+        Q, K, V, dO = f(q_h), f(k_h), f(v_h), f(do_h)
+        O, LSE = attention_fwd_rows(Q, K, V, scale, rows)
+        dQ = attention_bwd(Q[rows], K, V, dO[rows], scale)[0]
+        go, gl, gdq = o_h[b, h][rows].double().numpy(), l_h[b, h][rows].double().numpy(), dq_h[b, h][rows].double().numpy()
+        err["O"] = max(err["O"], float(np.abs(go - O).max() / np.abs(O).max()))
+        err["LSE"] = max(err["LSE"], float(np.abs(gl - LSE).max()))
+        err["dQ"] = max(err["dQ"], float(np.abs(gdq - dQ).max() / np.abs(dQ).max()))
+    tol = {"O": 2e-2, "LSE": 1e-3, "dQ": 5e-2}
+    return {"checked": f"O, LSE and dQ of {len(rows)} query rows in heads {heads} of the bench inputs",
+            "max_err": err, "tol": tol, "pass": all(err[k] <= tol[k] for k in tol)}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -568,6 +595,8 @@ def run_gpu(args):
         line["config"]["flop_count"] = "causal: half of 4*B*H*N^2*d forward, 2.5x that backward"
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = (cpu_baseline_causal if causal else cpu_baseline)(args.cpu_seconds)
+        if not causal:
+            line["cpu_baseline"]["parity_sample"] = parity_sample(q_h, k_h, v_h, do_h, o, lse, dq, scale)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
