@@ -572,12 +572,15 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const float* drow = stat_smem + st * (C::STAT_BYTES / 4) + C::BQ + 64 * g;
       // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, written over
       // this group's S^T columns (64 queries -> packed columns 64g..64g+31)
-      uint32_t pb[32];
+      // for the dV products; phase 2 takes the fp32 values, kept in
+      // registers (no unpacking, and dS from P before its rounding)
+      uint64_t pf[32];  // P of the 64 query columns as fp32 pairs
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t sr[32];
         tmem_ld32(lane_addr + C::COL_S + 64 * g + 32 * h, sr);
         tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
           // nl = -LSE*log2e of four query columns
@@ -593,14 +596,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             p2 = c + 2 < r_rel ? 0.f : p2;
             p3 = c + 3 < r_rel ? 0.f : p3;
           }
-          pb[16 * h + 2 * k4] = pack_bf16x2(p0, p1);
-          pb[16 * h + 2 * k4 + 1] = pack_bf16x2(p2, p3);
+          pf[16 * h + 2 * k4] = f2_pack(p0, p1);
+          pf[16 * h + 2 * k4 + 1] = f2_pack(p2, p3);
+          pk[2 * k4] = pack_bf16x2(p0, p1);
+          pk[2 * k4 + 1] = pack_bf16x2(p2, p3);
         }
+        tmem_st16(lane_addr + C::COL_S + 64 * g + 16 * h, pk);
       }
       // P^T of this group's 64 queries goes to the first 32 of its own S^T
       // columns (64g .. 64g+31), so neither group overwrites scores the
       // other has not read yet; the dV products take their A slices there.
-      tmem_st32(lane_addr + C::COL_S + 64 * g, pb);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -623,12 +628,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           // nd = -D of four query columns; dS' = P * (dP - D). The softmax
           // scale of dS is applied once to dK (epilogue) and dQ (convert).
           const float4 nd = *reinterpret_cast<const float4*>(drow + 32 * h + 4 * k4);
-          const float2 pa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[16 * h + 2 * k4]));
-          const float2 pc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pb[16 * h + 2 * k4 + 1]));
           const uint64_t ta = fadd2(f2_pack(__uint_as_float(dr[4 * k4]), __uint_as_float(dr[4 * k4 + 1])), f2_pack(nd.x, nd.y));
           const uint64_t tb = fadd2(f2_pack(__uint_as_float(dr[4 * k4 + 2]), __uint_as_float(dr[4 * k4 + 3])), f2_pack(nd.z, nd.w));
-          const float2 ga = f2_unpack(fmul2(f2_pack(pa.x, pa.y), ta));
-          const float2 gb = f2_unpack(fmul2(f2_pack(pc.x, pc.y), tb));
+          const float2 ga = f2_unpack(fmul2(pf[16 * h + 2 * k4], ta));
+          const float2 gb = f2_unpack(fmul2(pf[16 * h + 2 * k4 + 1], tb));
           dk[2 * k4] = pack_bf16x2(ga.x, ga.y);
           dk[2 * k4 + 1] = pack_bf16x2(gb.x, gb.y);
         }
