@@ -139,10 +139,9 @@ def bf16_peak(peaks, src, clocks, timed_seconds):
 
 def fwd_kernel_name(B, H, N, D, sms):
     """The forward kernel a bf16 fixed-length problem runs on, on a GPU with
-    `sms` SMs, by the routing rule fa.h documents for fa_fwd_plan: d = 64,
-    N <= 8192 and B*H*ceil(N/512) >= 3/4 of the SMs take the four-query-tile
-    kernel."""
-    if D == 64 and N <= 8192 and 4 * B * H * (-(-N // 512)) >= 3 * sms:
+    `sms` SMs, by the routing rule fa.h documents for fa_fwd_plan: d = 64
+    and B*H*ceil(N/512) >= 3/4 of the SMs take the four-query-tile kernel."""
+    if D == 64 and 4 * B * H * (-(-N // 512)) >= 3 * sms:
         return "fwd_bf16_q4_kernel"
     return f"fwd_bf16_kernel<{D}>"
 

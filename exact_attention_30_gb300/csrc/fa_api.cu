@@ -243,13 +243,12 @@ unsigned long long clamp_limit(long long limit_ns) {
 
 // The bf16 forward at d = 64 runs on the four-query-tile kernel (one CTA per
 // batch*head and 512-row block) when the problem is fixed-length (causal or
-// not), its grid fills at least three quarters of the GPU's resident CTAs
+// not) and its grid fills at least three quarters of the GPU's resident CTAs
 // (fewer CTAs leave too many SMs idle; the two-tile kernel's grid, twice as
-// large and split at its tail, then finishes first) and N <= 8192 (on longer
-// sequences the two kernels are level). Everything else runs on the two-tile
-// kernel. `slots`: forward CTAs resident at once (the SM count).
+// large and split at its tail, then finishes first). Everything else runs on
+// the two-tile kernel. `slots`: forward CTAs resident at once (the SM count).
 bool fwd_uses_q4(const SeqArgs& sq, int BH, int d, fa_dtype dt, int slots) {
-  if (dt != FA_BF16 || d != 64 || sq.cu_seqlens != nullptr || sq.N > 8192) return false;
+  if (dt != FA_BF16 || d != 64 || sq.cu_seqlens != nullptr) return false;
   const long long ctas = (long long)BH * ((sq.N + 511) / 512);
   return 4 * ctas >= 3ll * slots;
 }

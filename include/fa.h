@@ -101,7 +101,7 @@ size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int flags, fa_dtype dt
  * units of the last wave are split into min(W / (U mod W), 4, key tiles / 4)
  * ranges when that is at least 2 and U >= W (bf16, non-causal only).
  * bf16 d = 64 problems that run on the four-query-tile kernel (causal or
- * not, N <= 8192, B*H*ceil(N/512) >= 3/4 of W) are never split.
+ * not, B*H*ceil(N/512) >= 3/4 of W) are never split.
  * Errors: FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED (as fa_fwd_ex).
  */
 fa_status fa_fwd_plan(int B, int H, int N, int d, int flags, fa_dtype dt, int resident_ctas,

@@ -141,7 +141,7 @@ def _tail_makespan(units, slots, n_full, n_tail, splits):
     (2, 16, 4096, 128, 152), (1, 32, 16384, 128, 152), (4, 16, 1024, 64, 152),
     (1, 10, 4096, 128, 152), (1, 10, 4000, 64, 152), (1, 4, 4096, 128, 152),
     (1, 200, 1024, 128, 152), (1, 200, 256, 128, 152), (3, 7, 777, 64, 148), (1, 1, 1, 128, 152),
-    (2, 16, 4096, 64, 152), (1, 16, 16384, 64, 152)])
+    (2, 16, 4096, 64, 152), (1, 16, 16384, 64, 152), (1, 2, 20000, 64, 152)])
 def test_forward_tail_split_plan_on_the_host(lib, B, H, N, d, slots):
     """The forward's tail split covers every unit once, splits only the last,
     partly filled wave (never with fewer than four key tiles per range, at
@@ -152,8 +152,8 @@ def test_forward_tail_split_plan_on_the_host(lib, B, H, N, d, slots):
     nf, nt, sp = fa.fa_fwd_plan(B, H, N, d, resident_ctas=slots)
     assert nf + nt == units and sp >= 1 and (sp == 1) == (nt == 0)
     # d = 64 problems whose four-tile grid (one CTA per 512 rows) fills at
-    # least 3/4 of the resident CTAs, N <= 8192, run unsplit on that kernel
-    if d == 64 and N <= 8192 and 4 * B * H * -(-N // 512) >= 3 * slots:
+    # least 3/4 of the resident CTAs run unsplit on that kernel
+    if d == 64 and 4 * B * H * -(-N // 512) >= 3 * slots:
         assert (nf, nt, sp) == (units, 0, 1)
     elif sp > 1:
         assert nt == units % slots and units >= slots

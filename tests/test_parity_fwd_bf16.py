@@ -119,9 +119,9 @@ def test_outputs_written_everywhere_and_nowhere_else():
 
 def _runs_on_four_tile_kernel(B, H, N, d):
     """The routing rule fa.h states for fa_fwd_plan: bf16, d = 64, causal or not,
-    N <= 8192 and B*H*ceil(N/512) >= 3/4 of the SMs."""
+    B*H*ceil(N/512) >= 3/4 of the SMs."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return d == 64 and N <= 8192 and 4 * B * H * -(-N // 512) >= 3 * sms
+    return d == 64 and 4 * B * H * -(-N // 512) >= 3 * sms
 
 
 @pytest.mark.parametrize("N,H", [(1, 160), (63, 160), (64, 160), (65, 160), (300, 160), (511, 160),
@@ -192,3 +192,28 @@ def test_four_tile_d64_causal_forward(N, H):
         O, LSE = attention_fwd(q64[0, h], k64[0, h], v64[0, h], scale, causal=True)
         assert rel_max(o64[0, h], O) <= TOL_BF16_O, h
         assert max_abs(l64[0, h], LSE) <= TOL_BF16_LSE, h
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(1, 16, 16384, False), (1, 16, 16384, True), (1, 32, 12289, False),
+                                          (1, 8, 32768, True)])
+def test_four_tile_d64_long_sequences(B, H, N, causal):
+    """Long sequences on the four-query-tile d = 64 kernel: sampled rows of
+    every head (the first and last rows of every 512-row block among them, and
+    the ragged tail) against the oracle, causal or not."""
+    d = 64
+    assert _runs_on_four_tile_kernel(B, H, N, d)
+    q, k, v, _ = random_qkv(B, H, N, d, torch.bfloat16, seed=N + H + int(causal), with_do=False)
+    scale = 1 / math.sqrt(d)
+    o, lse = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), scale, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    q64, k64, v64 = to64(q), to64(k), to64(v)
+    o64, l64 = to64(o), to64(lse)
+    rng = np.random.default_rng(N)
+    edges = np.concatenate([np.arange(0, N, 512), np.arange(511, N, 512), [N - 1]])
+    for h in range(H):
+        rows = np.unique(np.concatenate([edges[h % 2::2], rng.choice(N, 16, replace=False)]))
+        O, LSE = attention_fwd_rows(q64[0, h], k64[0, h], v64[0, h], scale, rows, causal=causal)
+        assert rel_max(o64[0, h][rows], O) <= TOL_BF16_O, h
+        assert max_abs(l64[0, h][rows], LSE) <= TOL_BF16_LSE, h
