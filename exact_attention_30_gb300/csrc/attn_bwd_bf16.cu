@@ -13,9 +13,11 @@
 //  1. bwd_pre:   -D and -LSE*log2(e) per row into the workspace (rows
 //                padded to a multiple of 128: 0 and -inf past N, which makes
 //                P = 0 there), and zero the fp32 dQ accumulator.
-//  2. bwd_main:  one CTA per (batch*head, 128-key tile j); K_j, V_j stay in
+//  2. bwd_main:  per unit (batch*head, 128-key tile j): K_j, V_j stay in
 //                shared memory while 128-query tiles i stream through a TMA
-//                ring. All products run on tcgen05 with fp32 accumulators in
+//                ring. Fixed-length, non-causal problems run a persistent
+//                grid (one CTA per SM walking the units); causal and packed
+//                batches one CTA per unit. All products run on tcgen05 with fp32 accumulators in
 //                TMEM (every MMA M = N = 128):
 //                  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T   (recompute; keys on lanes)
 //                  dV += P^T dO_i (P^T read from TMEM), dK += dS^T Q_i
@@ -27,7 +29,8 @@
 //                bf16 dS^T into a swizzled shared-memory tile that feeds both
 //                dK (K-major view) and dQ (MN-major view). dQ_i is computed
 //                into the dP^T columns; a dQ warpgroup reads it out and adds
-//                it to the accumulator as above. Per query tile the
+//                it to the accumulator as above. dV_j and dK_j leave TMEM
+//                through a staging pass that stores whole 128-byte rows. Per query tile the
 //                MMA order is dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1), so the
 //                next tile's recompute overlaps this tile's softmax.
 //  3. dq_convert: fp32 accumulator times scale -> bf16 dQ.
@@ -183,6 +186,11 @@ struct BwdCfg {
   // dQ = dS K (queries on the lanes; an M = 64 product would be needed
   // otherwise) and stages each lane's row through a swizzled block
   static constexpr bool DQ_T = (D == 128);
+  // Who writes an item's dV and dK: at d = 64 the dQ warps (lightly loaded
+  // there; the softmax warps go straight on to the next item), at d = 128
+  // the softmax warps (the dQ warps' read-out of 128 columns per tile is on
+  // the critical loop). Both measured; each is the faster one at its d.
+  static constexpr bool EPI_DQ = (D == 64);
   static constexpr int CH = D / 64;                  // 128-byte chunks per K/V/Q/dO row
   // Q_i (with its LSE/D statistics) is read by S^T(i), issued one tile
   // early, and last by dK(i); dO_i by dP^T(i), also issued one tile early,
@@ -213,8 +221,8 @@ struct BwdCfg {
   static_assert(OFF_DQS % 1024 == 0, "swizzled staging alignment");
   // barriers: kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], st_full[2],
   //           st_empty[2], s_full, dp_full, pt_ready, ds_ready, ds_empty, dq_full,
-  //           dq_empty, acc_done, drain
-  static constexpr int NBAR = 1 + 2 * QSTAGES + 2 * DOSTAGES + 2 * STATSTAGES + 9;
+  //           dq_empty, acc_done, drain, kv_empty, acc_empty
+  static constexpr int NBAR = 1 + 2 * QSTAGES + 2 * DOSTAGES + 2 * STATSTAGES + 11;
   static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int SMEM_MAX = 227 * 1024;
   // request 1 KB of alignment slack when it fits; the kernel checks alignment
@@ -232,6 +240,74 @@ struct BwdCfg {
   static_assert(BQ == bwd_query_tile(D), "host tensor-map box height");
 };
 
+// One work item of the main kernel: a unit (batch*head, 128-key tile), or one
+// query range of a split unit.
+struct BwdItem {
+  SeqView sv;
+  int kb;         // key tile
+  int i_begin;    // first query tile
+  int n_it;       // query tiles
+  int tail_unit;  // index among the split units, or -1
+  int part;       // query range of a split unit
+};
+
+// Item w of the 1-D item list (fixed length, non-causal: units key tile
+// fastest, those from n_full on as `splits` query ranges each), or, with
+// list == false, this CTA's unit of the 2-D/3-D grids (variable length,
+// causal). False: nothing to do (a head past the last one, a key tile past
+// the sequence's end). Out of line: every role decodes each of its items, and
+// one shared copy keeps the kernel's code (and instruction-cache footprint)
+// small.
+template <int BK, int BQ>
+__device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdItem& it) {
+  const bool causal = a.seq.causal != 0;
+  int bh;
+  it.tail_unit = -1;
+  it.part = 0;
+  if (list) {
+    const int kblocks = (a.seq.N + BK - 1) / BK;
+    int u = w;
+    if (u >= a.n_full) {
+      const int r = u - a.n_full;
+      it.tail_unit = r / a.splits;
+      it.part = r - it.tail_unit * a.splits;
+      u = a.n_full + it.tail_unit;
+    }
+    bh = u / kblocks;
+    it.kb = u - bh * kblocks;
+  } else {
+    // causal grids: (heads of a group, key tiles in increasing order = most
+    // query tiles first, head groups)
+    bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
+    it.kb = causal ? (int)blockIdx.y : (int)blockIdx.x;
+  }
+  if (bh >= a.BH) return false;
+  it.sv = seq_view(a.seq, bh, a.status);
+  const int N = it.sv.len;  // queries = keys of this sequence
+  if (it.kb * BK >= N) return false;
+  // query tiles i_begin .. i_end-1: all of them, those at or after the
+  // diagonal (causal: the earlier ones see no key of this tile), or this
+  // item's range of a split unit
+  const int n_q = (N + BQ - 1) / BQ;
+  int i_end = n_q;
+  it.i_begin = causal ? it.kb : 0;
+  if (it.tail_unit >= 0) {  // part < splits <= 4: no overflow
+    it.i_begin = it.part * n_q / a.splits;
+    i_end = (it.part + 1) * n_q / a.splits;
+  }
+  it.n_it = i_end - it.i_begin;
+  return it.n_it > 0;
+}
+
+// Fixed-length, non-causal problems run as a persistent grid (a.items > 0):
+// one CTA per SM walks the item list with stride gridDim.x, so the set-up,
+// the TMEM allocation and the CTA turnaround are paid once per SM, and the
+// next item's first loads and products overlap this item's last tile and
+// epilogue. Every role walks the same items; the rings and the per-tile
+// barriers continue across items (global tile index g), the K/V tile and the
+// dV/dK accumulators are handed over per item (kv_empty; the next item's
+// first dV and dK products come after the softmax warps' epilogue, which
+// precedes their next pt_ready and ds_ready arrivals).
 template <int D>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
@@ -252,52 +328,23 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             B_STEMPTY = B_STFULL + C::STATSTAGES, B_SFULL = B_STEMPTY + C::STATSTAGES,
             B_DPFULL = B_SFULL + 1, B_PTREADY = B_SFULL + 2, B_DSREADY = B_SFULL + 3,
             B_DSEMPTY = B_SFULL + 4, B_DQFULL = B_SFULL + 5, B_DQEMPTY = B_SFULL + 6,
-            B_ACC = B_SFULL + 7, B_DRAIN = B_SFULL + 8;
+            B_ACC = B_SFULL + 7, B_DRAIN = B_SFULL + 8, B_KVEMPTY = B_SFULL + 9,
+            B_ACCEMPTY = B_SFULL + 10;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   const float* stat_smem = reinterpret_cast<const float*>(smem + C::OFF_STAT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
-  int bh, kb;
-  int tail_unit = -1, part = 0;  // split units: index among them, query range
-  if (a.splits > 1) {
-    // tail-split grid (fixed length, non-causal): one CTA per unit
-    // (batch*head, key tile), key tile fastest; the units from n_full on
-    // run as a.splits query ranges, one CTA each
-    const int kblocks = (a.seq.N + C::BK - 1) / C::BK;
-    int u = (int)blockIdx.x;
-    if (u >= a.n_full) {
-      const int r = u - a.n_full;
-      tail_unit = r / a.splits;
-      part = r - tail_unit * a.splits;
-      u = a.n_full + tail_unit;
-    }
-    bh = u / kblocks;
-    kb = u - bh * kblocks;
-  } else {
-    // causal grids: (heads of a group, key tiles in increasing order = most
-    // query tiles first, head groups)
-    bh = causal ? (int)(blockIdx.z * gridDim.x + blockIdx.x) : (int)blockIdx.y;
-    kb = causal ? (int)blockIdx.y : (int)blockIdx.x;
+  const bool list = a.items > 0;
+  const int w_first = list ? (int)blockIdx.x : 0;
+  const int w_step = list ? (int)gridDim.x : 1;
+  const int w_end = list ? a.items : 1;
+  if (w_first >= w_end) return;
+  if (!list) {
+    BwdItem it0;
+    if (!bwd_item<C::BK, C::BQ>(a, false, 0, it0)) return;  // no key of a sequence here
   }
-  if (bh >= a.BH) return;  // past the last head of the last group
-  const SeqView sv = seq_view(a.seq, bh, a.status);
-  const int N = sv.len;  // queries = keys of this sequence
-  const int k0 = kb * C::BK;
-  if (k0 >= N) return;  // the whole CTA: no key of this sequence here
-  const int n_q = (N + C::BQ - 1) / C::BQ;
-  // query tiles i_begin .. i_end-1: all of them, those at or after the
-  // diagonal (causal: the earlier ones see no key of this tile), or this
-  // CTA's range of a split unit
-  int i_begin = causal ? kb : 0, i_end = n_q;
-  if (tail_unit >= 0) {
-    i_begin = (int)((long long)part * n_q / a.splits);
-    i_end = (int)((long long)(part + 1) * n_q / a.splits);
-  }
-  const int n_it = i_end - i_begin;  // >= 1
-  const int y0 = sv.start, plane = sv.plane;
-  const size_t ws_row0 = (size_t)plane * a.ws_rows + (size_t)y0;  // workspace row of query 0
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(B_KV), 1);
@@ -322,6 +369,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_init(BAR(B_DQEMPTY), 4);  // one arrival per dQ warp
     mbar_init(BAR(B_ACC), 1);
     mbar_init(BAR(B_DRAIN), 1);
+    mbar_init(BAR(B_KVEMPTY), 1);
+    mbar_init(BAR(B_ACCEMPTY), 4);  // one arrival per dQ warp, after its epilogue
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -337,28 +386,51 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tma_prefetch_desc(&a.tmQ);
       tma_prefetch_desc(&a.tmK);
       tma_prefetch_desc(&a.tmV);
-      mbar_arrive_expect_tx(BAR(B_KV), 2 * C::TILE);
-      for (int c = 0; c < C::CH; ++c) {
-        tma_load_3d(sbase + C::OFF_K + c * C::ROW_CHUNK, &a.tmK, BAR(B_KV), c * 64, y0 + k0, plane);
-        tma_load_3d(sbase + C::OFF_V + c * C::ROW_CHUNK, &a.tmV, BAR(B_KV), c * 64, y0 + k0, plane);
-      }
-      int last[C::QSTAGES];
+      int last[C::QSTAGES];  // global tile index of the last load into each slot
 #pragma unroll
       for (int s = 0; s < C::QSTAGES; ++s) last[s] = -1;
-      for (int i = 0; i < n_it; ++i) {  // i: iteration; query tile i_begin + i
-        if (*abort_flag) break;
-        const int s = i % C::QSTAGES;
-        const uint32_t ph = (i / C::QSTAGES) & 1;
-        if (!mbar_wait(BAR(B_QEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) { *abort_flag = 1; break; }
-        if (i != a.debug_skip_q) {
-          mbar_arrive_expect_tx(BAR(B_QFULL + s), C::TILE);
-          for (int c = 0; c < C::CH; ++c)
-            tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
-                        c * 64, y0 + (i_begin + i) * C::BQ, plane);
-          last[s] = i;
+      int ui = 0, g0 = 0;  // items and query tiles before this item
+      bool ok = true;
+      for (int w = w_first; ok && w < w_end; w += w_step) {
+        BwdItem it;
+        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        const int plane = it.sv.plane, qrow0 = it.sv.start + it.i_begin * C::BQ;
+        auto load_q = [&](int i) {  // query tile i_begin + i into its ring slot
+          const int g = g0 + i;
+          const int s = g % C::QSTAGES;
+          if (!mbar_wait(BAR(B_QEMPTY + s), ((g / C::QSTAGES) & 1) ^ 1, a.status, a.wait_limit_ns)) return false;
+          if (g != a.debug_skip_q) {
+            mbar_arrive_expect_tx(BAR(B_QFULL + s), C::TILE);
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(sbase + C::OFF_Q + s * C::TILE + c * C::ROW_CHUNK, &a.tmQ, BAR(B_QFULL + s),
+                          c * 64, qrow0 + i * C::BQ, plane);
+            last[s] = g;
+          }
+          return true;
+        };
+        int i = 0;
+        if (ui > 0) {
+          // The slots of this item's first QSTAGES-1 query tiles were
+          // released by dK products issued before the previous item's last
+          // dQ, so they load ahead of K and V, which wait for that dQ.
+          for (; ok && i < it.n_it && i < C::QSTAGES - 1; ++i) ok = *abort_flag == 0 && load_q(i);
+          ok = ok && mbar_wait(BAR(B_KVEMPTY), (ui - 1) & 1, a.status, a.wait_limit_ns);
+          if (!ok) break;
         }
+        mbar_arrive_expect_tx(BAR(B_KV), 2 * C::TILE);
+        for (int c = 0; c < C::CH; ++c) {
+          tma_load_3d(sbase + C::OFF_K + c * C::ROW_CHUNK, &a.tmK, BAR(B_KV), c * 64,
+                      it.sv.start + it.kb * C::BK, plane);
+          tma_load_3d(sbase + C::OFF_V + c * C::ROW_CHUNK, &a.tmV, BAR(B_KV), c * 64,
+                      it.sv.start + it.kb * C::BK, plane);
+        }
+        ++ui;
+        for (; ok && i < it.n_it; ++i) ok = *abort_flag == 0 && load_q(i);
+        g0 += it.n_it;
       }
-      mbar_wait(BAR(B_KV), 0, a.status, a.wait_limit_ns);
+      if (!ok) *abort_flag = 1;
+      // drain: the last load issued into each buffer must have landed before exit
+      if (ui > 0) mbar_wait(BAR(B_KV), (ui - 1) & 1, a.status, a.wait_limit_ns);
 #pragma unroll
       for (int s = 0; s < C::QSTAGES; ++s)
         if (last[s] >= 0) mbar_wait(BAR(B_QFULL + s), (last[s] / C::QSTAGES) & 1, a.status, a.wait_limit_ns);
@@ -374,56 +446,67 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     // sequence, so that P = 0 there. Lane 0 issues the dO tile loads.
     const bool stat_bulk = a.seq.cu_seqlens == nullptr;  // rows 16-byte aligned, padded
     if (lane == 0) tma_prefetch_desc(&a.tmdO);
-    int last = -1;       // lane 0: last dO tile issued
+    int last = -1;       // lane 0: global tile index of the last dO tile issued
     int last_stat = -1;  // lane 0: last statistics tile issued by bulk copies
-    for (int i = 0; i < n_it; ++i) {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      {
-        const int t = i % C::STATSTAGES;
-        const uint32_t pt = (i / C::STATSTAGES) & 1;
-        if (!mbar_wait_warp(BAR(B_STEMPTY + t), pt ^ 1, a.status, a.wait_limit_ns)) {
-          if (lane == 0) *abort_flag = 1;
-          break;
-        }
-        const int q_row = (i_begin + i) * C::BQ;  // first query row of the tile, within the sequence
-        if (stat_bulk) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(BAR(B_STFULL + t), C::STAT_BYTES);
-            bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES, a.lse2 + ws_row0 + q_row, C::BQ * 4,
-                      BAR(B_STFULL + t));
-            bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES + C::BQ * 4, a.Drow + ws_row0 + q_row,
-                      C::BQ * 4, BAR(B_STFULL + t));
-            last_stat = i;
+    int g0 = 0;
+    bool ok = true;
+    for (int w = w_first; ok && w < w_end; w += w_step) {
+      BwdItem it;
+      if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+      const int N = it.sv.len, plane = it.sv.plane;
+      const size_t ws_row0 = (size_t)plane * a.ws_rows + (size_t)it.sv.start;  // workspace row of query 0
+      for (int i = 0; i < it.n_it; ++i) {
+        const int g = g0 + i;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+        const int q_row = (it.i_begin + i) * C::BQ;  // first query row of the tile, within the sequence
+        {
+          const int t = g % C::STATSTAGES;
+          const uint32_t pt = (g / C::STATSTAGES) & 1;
+          if (!mbar_wait_warp(BAR(B_STEMPTY + t), pt ^ 1, a.status, a.wait_limit_ns)) {
+            if (lane == 0) *abort_flag = 1;
+            ok = false;
+            break;
           }
-        } else {
-          const size_t row0 = ws_row0 + (size_t)q_row + 4 * lane;
-          const int live = N - q_row - 4 * lane;  // rows of this lane inside the sequence
-          float* dst = reinterpret_cast<float*>(smem + C::OFF_STAT + t * C::STAT_BYTES) + 4 * lane;
-          const float4 l4 = make_float4(live > 0 ? a.lse2[row0] : -INFINITY,
-                                        live > 1 ? a.lse2[row0 + 1] : -INFINITY,
-                                        live > 2 ? a.lse2[row0 + 2] : -INFINITY,
-                                        live > 3 ? a.lse2[row0 + 3] : -INFINITY);
-          const float4 d4 = make_float4(a.Drow[row0], a.Drow[row0 + 1], a.Drow[row0 + 2], a.Drow[row0 + 3]);
-          *reinterpret_cast<float4*>(dst) = l4;
-          *reinterpret_cast<float4*>(dst + C::BQ) = d4;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_STFULL + t));
+          if (stat_bulk) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(BAR(B_STFULL + t), C::STAT_BYTES);
+              bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES, a.lse2 + ws_row0 + q_row, C::BQ * 4,
+                        BAR(B_STFULL + t));
+              bulk_load(sbase + C::OFF_STAT + t * C::STAT_BYTES + C::BQ * 4, a.Drow + ws_row0 + q_row,
+                        C::BQ * 4, BAR(B_STFULL + t));
+              last_stat = g;
+            }
+          } else {
+            const size_t row0 = ws_row0 + (size_t)q_row + 4 * lane;
+            const int live = N - q_row - 4 * lane;  // rows of this lane inside the sequence
+            float* dst = reinterpret_cast<float*>(smem + C::OFF_STAT + t * C::STAT_BYTES) + 4 * lane;
+            const float4 l4 = make_float4(live > 0 ? a.lse2[row0] : -INFINITY,
+                                          live > 1 ? a.lse2[row0 + 1] : -INFINITY,
+                                          live > 2 ? a.lse2[row0 + 2] : -INFINITY,
+                                          live > 3 ? a.lse2[row0 + 3] : -INFINITY);
+            const float4 d4 = make_float4(a.Drow[row0], a.Drow[row0 + 1], a.Drow[row0 + 2], a.Drow[row0 + 3]);
+            *reinterpret_cast<float4*>(dst) = l4;
+            *reinterpret_cast<float4*>(dst + C::BQ) = d4;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_STFULL + t));
+          }
         }
-      }
-      if (lane == 0) {
-        const int s = i % C::DOSTAGES;
-        const uint32_t ph = (i / C::DOSTAGES) & 1;
-        if (!mbar_wait(BAR(B_DOEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) {
-          *abort_flag = 1;
-        } else {
-          mbar_arrive_expect_tx(BAR(B_DOFULL + s), C::TILE);
-          for (int c = 0; c < C::CH; ++c)
-            tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
-                        BAR(B_DOFULL + s), c * 64, y0 + (i_begin + i) * C::BQ, plane);
-          last = i;
+        if (lane == 0) {
+          const int s = g % C::DOSTAGES;
+          const uint32_t ph = (g / C::DOSTAGES) & 1;
+          if (!mbar_wait(BAR(B_DOEMPTY + s), ph ^ 1, a.status, a.wait_limit_ns)) {
+            *abort_flag = 1;
+          } else {
+            mbar_arrive_expect_tx(BAR(B_DOFULL + s), C::TILE);
+            for (int c = 0; c < C::CH; ++c)
+              tma_load_3d(sbase + C::OFF_DO + s * C::TILE + c * C::ROW_CHUNK, &a.tmdO,
+                          BAR(B_DOFULL + s), c * 64, it.sv.start + q_row, plane);
+            last = g;
+          }
         }
+        __syncwarp();
       }
-      __syncwarp();
+      g0 += it.n_it;
     }
     if (lane == 0) {
       // the last dO and statistics copies issued into each slot must have
@@ -495,50 +578,73 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           else mma_ss(tmem + C::COL_DP, dSmn + roff(kk), dKmn + roff(kk), id_dq, kk > 0, leader);
         }
       };
-      bool ok = wait(B_KV, 0) &&
-                wait(B_QFULL + 0, 0) &&
-                wait(B_DOFULL + 0, 0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        mma_commit(BAR(B_SFULL), leader);
-        issue_dp(0);  // dO ring slot 0
-        mma_commit(BAR(B_DPFULL), leader);
-      }
-      for (int i = 0; ok && i < n_it; ++i) {
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-        const int s = i % C::QSTAGES, so = i % C::DOSTAGES;
-        const bool more = i + 1 < n_it;
-        const int s1 = (i + 1) % C::QSTAGES, so1 = (i + 1) % C::DOSTAGES;
-        const uint32_t ph1 = ((i + 1) / C::QSTAGES) & 1, pho1 = ((i + 1) / C::DOSTAGES) & 1;
-        if (!wait(B_PTREADY, i & 1)) { ok = false; break; }
-        tc_fence_after();
-        issue_dv(so, i > 0);
-        mma_commit(BAR(B_DOEMPTY + so), leader);  // dO_i: last use was dV
-        if (more) {
-          if (!wait(B_QFULL + s1, ph1)) { ok = false; break; }
+      bool ok = true;
+      int ui = 0, g0 = 0;  // items and query tiles before this item
+      for (int w = w_first; ok && w < w_end; w += w_step) {
+        BwdItem it;
+        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        const int n_it = it.n_it;
+        {
+          // the item's first S^T and dP^T (S^T overwrites P^T of the previous
+          // item's last tile: ordered after the dV products that read it)
+          const int s = g0 % C::QSTAGES, so = g0 % C::DOSTAGES;
+          ok = wait(B_KV, ui & 1) && wait(B_QFULL + s, (g0 / C::QSTAGES) & 1);
+          if (!ok) break;
           tc_fence_after();
-          issue_s(s1);  // overwrites P^T(i): ordered after the dV products that read it
+          issue_s(s);
           mma_commit(BAR(B_SFULL), leader);
-        }
-        if (!wait(B_DSREADY, i & 1)) { ok = false; break; }
-        tc_fence_after();
-        issue_dq();  // the dP^T columns: dP^T(i) was consumed before ds_ready
-        mma_commit(BAR(B_DQFULL), leader);
-        issue_dk(s, i > 0);
-        mma_commit(BAR(B_QEMPTY + s), leader);  // Q_i: last use was dK
-        mma_commit(BAR(B_DSEMPTY), leader);     // dS^T(i): last use was dQ/dK
-        if (more) {
-          // dP^T(i+1) reuses the dQ columns once the dQ warps have read dQ(i)
-          if (!wait(B_DQEMPTY, i & 1) ||
-              !wait(B_DOFULL + so1, pho1)) { ok = false; break; }
+          // dP^T reuses the dQ columns once the dQ warps have read the
+          // previous tile's dQ
+          ok = (g0 == 0 || wait(B_DQEMPTY, (g0 - 1) & 1)) && wait(B_DOFULL + so, (g0 / C::DOSTAGES) & 1);
+          if (!ok) break;
           tc_fence_after();
-          issue_dp(so1);
+          issue_dp(so);
           mma_commit(BAR(B_DPFULL), leader);
         }
+        for (int i = 0; i < n_it; ++i) {  // i: iteration; query tile i_begin + i; g: ring position
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+          const int g = g0 + i;
+          const int s = g % C::QSTAGES, so = g % C::DOSTAGES;
+          const bool more = i + 1 < n_it;
+          const int s1 = (g + 1) % C::QSTAGES, so1 = (g + 1) % C::DOSTAGES;
+          const uint32_t ph1 = ((g + 1) / C::QSTAGES) & 1, pho1 = ((g + 1) / C::DOSTAGES) & 1;
+          if (!wait(B_PTREADY, g & 1)) { ok = false; break; }
+          // the first dV (and dK) product of a later item overwrites the
+          // accumulators once the dQ warps have written the previous item's
+          // (softmax-warp epilogue: their pt_ready arrivals follow it)
+          if (C::EPI_DQ && i == 0 && ui > 0 && !wait(B_ACCEMPTY, (ui - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_dv(so, i > 0);
+          mma_commit(BAR(B_DOEMPTY + so), leader);  // dO_i: last use was dV
+          if (more) {
+            if (!wait(B_QFULL + s1, ph1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(s1);  // overwrites P^T(i): ordered after the dV products that read it
+            mma_commit(BAR(B_SFULL), leader);
+          }
+          if (!wait(B_DSREADY, g & 1)) { ok = false; break; }
+          tc_fence_after();
+          issue_dq();  // the dP^T columns: dP^T(i) was consumed before ds_ready
+          mma_commit(BAR(B_DQFULL), leader);
+          if (!more) mma_commit(BAR(B_KVEMPTY), leader);  // K, V: last uses were dQ and dP^T of this tile
+          issue_dk(s, i > 0);
+          mma_commit(BAR(B_QEMPTY + s), leader);  // Q_i: last use was dK
+          mma_commit(BAR(B_DSEMPTY), leader);     // dS^T(i): last use was dQ/dK
+          if (more) {
+            // dP^T(i+1) reuses the dQ columns once the dQ warps have read dQ(i)
+            if (!wait(B_DQEMPTY, g & 1) ||
+                !wait(B_DOFULL + so1, pho1)) { ok = false; break; }
+            tc_fence_after();
+            issue_dp(so1);
+            mma_commit(BAR(B_DPFULL), leader);
+          }
+        }
+        if (!ok) break;
+        mma_commit(BAR(B_ACC), leader);  // the item's dV and dK are complete
+        g0 += n_it;
+        ++ui;
       }
-      if (ok) mma_commit(BAR(B_ACC), leader);
-      else if (lane == 0) *abort_flag = 1;
+      if (!ok && lane == 0) *abort_flag = 1;
       mma_commit(BAR(B_DRAIN), leader);
       wait(B_DRAIN, 0);
     }
@@ -549,156 +655,192 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     const int g = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row within the tile == TMEM lane
-    const bool key_live = k0 + r < N;
     const int qc0 = 64 * g;  // first query column of this group
     const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
     const uint64_t c22 = f2_pack(a.scale_log2, a.scale_log2);
-    const float scale = a.scale;
     uint8_t* dsrow = smem + C::OFF_DS + g * C::ROW_CHUNK + r * 128;  // this group's dS^T chunk
     bool ok = true;
-    for (int i = 0; i < n_it; ++i) {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-      const int st = i % C::STATSTAGES;
-      // On the causal diagonal, P = 0 in the columns q < r (key r after query
-      // q): column 32h + 4k4 + e of this group is masked when it is below
-      // r - 64g. (Queries past the sequence have -LSE*log2e = -inf: P = 0.)
-      const bool diag = causal && i_begin + i == kb;
-      const int r_rel = r - qc0;
-      bool w = mbar_wait(BAR(B_SFULL), i & 1, a.status, a.wait_limit_ns) &&
-               mbar_wait(BAR(B_STFULL + st), (i / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
-      const float* lse2 = stat_smem + st * (C::STAT_BYTES / 4) + 64 * g;
-      const float* drow = stat_smem + st * (C::STAT_BYTES / 4) + C::BQ + 64 * g;
-      // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, written over
-      // this group's S^T columns (64 queries -> packed columns 64g..64g+31)
-      // for the dV products; phase 2 takes the fp32 values, kept in
-      // registers (no unpacking, and dS from P before its rounding)
-      uint64_t pf[32];  // P of the 64 query columns as fp32 pairs
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t sr[32];
-        tmem_ld32(lane_addr + C::COL_S + 64 * g + 32 * h, sr);
-        tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          // nl = -LSE*log2e of four query columns
-          const float4 nl = *reinterpret_cast<const float4*>(lse2 + 32 * h + 4 * k4);
-          const float2 xa = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4]), __uint_as_float(sr[4 * k4 + 1])), c22, f2_pack(nl.x, nl.y)));
-          const float2 xb = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4 + 2]), __uint_as_float(sr[4 * k4 + 3])), c22, f2_pack(nl.z, nl.w)));
-          float p0 = ex2_approx(xa.x), p1 = ex2_approx(xa.y), p2 = ex2_approx(xb.x), p3 = ex2_approx(xb.y);
-          if (!key_live) p0 = p1 = p2 = p3 = 0.f;
-          if (diag) {
-            const int c = 32 * h + 4 * k4;
-            p0 = c < r_rel ? 0.f : p0;
-            p1 = c + 1 < r_rel ? 0.f : p1;
-            p2 = c + 2 < r_rel ? 0.f : p2;
-            p3 = c + 3 < r_rel ? 0.f : p3;
-          }
-          pf[16 * h + 2 * k4] = f2_pack(p0, p1);
-          pf[16 * h + 2 * k4 + 1] = f2_pack(p2, p3);
-          pk[2 * k4] = pack_bf16x2(p0, p1);
-          pk[2 * k4 + 1] = pack_bf16x2(p2, p3);
-        }
-        tmem_st16(lane_addr + C::COL_S + 64 * g + 16 * h, pk);
+    int ui = 0, g0 = 0;  // items and query tiles before this item
+    for (int w = w_first; ok && w < w_end; w += w_step) {
+      int n_it, diag_i;
+      bool key_live;
+      {
+        BwdItem it;
+        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        n_it = it.n_it;
+        diag_i = causal ? it.kb - it.i_begin : -1;  // iteration of the diagonal tile
+        key_live = it.kb * C::BK + r < it.sv.len;
       }
-      // P^T of this group's 64 queries goes to the first 32 of its own S^T
-      // columns (64g .. 64g+31), so neither group overwrites scores the
-      // other has not read yet; the dV products take their A slices there.
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_PTREADY));
-      // phase 2: dS'^T = P^T o (dP^T - D), bf16, into this group's swizzled
-      // [128 keys][64 queries] chunk of the dS^T tile (16-byte unit c of row r
-      // lands at unit c ^ (r & 7))
-      w = mbar_wait(BAR(B_DPFULL), i & 1, a.status, a.wait_limit_ns) &&
-          mbar_wait(BAR(B_DSEMPTY), (i & 1) ^ 1, a.status, a.wait_limit_ns);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
+      for (int i = 0; i < n_it; ++i) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+        const int gt = g0 + i;  // ring position of the tile
+        const int st = gt % C::STATSTAGES;
+        // On the causal diagonal, P = 0 in the columns q < r (key r after query
+        // q): column 32h + 4k4 + e of this group is masked when it is below
+        // r - 64g. (Queries past the sequence have -LSE*log2e = -inf: P = 0.)
+        const bool diag = i == diag_i;
+        const int r_rel = r - qc0;
+        bool w_ok = mbar_wait(BAR(B_SFULL), gt & 1, a.status, a.wait_limit_ns) &&
+                    mbar_wait(BAR(B_STFULL + st), (gt / C::STATSTAGES) & 1, a.status, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        tc_fence_after();
+        const float* lse2 = stat_smem + st * (C::STAT_BYTES / 4) + 64 * g;
+        const float* drow = stat_smem + st * (C::STAT_BYTES / 4) + C::BQ + 64 * g;
+        // phase 1: P^T = 2^(S^T * scale*log2e - LSE*log2e), bf16, written over
+        // this group's S^T columns (64 queries -> packed columns 64g..64g+31)
+        // for the dV products; phase 2 takes the fp32 values, kept in
+        // registers (no unpacking, and dS from P before its rounding)
+        uint64_t pf[32];  // P of the 64 query columns as fp32 pairs
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t dr[32];
-        tmem_ld32(lane_addr + C::COL_DP + 64 * g + 32 * h, dr);
-        tmem_ld_wait();
-        uint32_t dk[16];
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          // nd = -D of four query columns; dS' = P * (dP - D). The softmax
-          // scale of dS is applied once to dK (epilogue) and dQ (convert).
-          const float4 nd = *reinterpret_cast<const float4*>(drow + 32 * h + 4 * k4);
-          const uint64_t ta = fadd2(f2_pack(__uint_as_float(dr[4 * k4]), __uint_as_float(dr[4 * k4 + 1])), f2_pack(nd.x, nd.y));
-          const uint64_t tb = fadd2(f2_pack(__uint_as_float(dr[4 * k4 + 2]), __uint_as_float(dr[4 * k4 + 3])), f2_pack(nd.z, nd.w));
-          const float2 ga = f2_unpack(fmul2(pf[16 * h + 2 * k4], ta));
-          const float2 gb = f2_unpack(fmul2(pf[16 * h + 2 * k4 + 1], tb));
-          dk[2 * k4] = pack_bf16x2(ga.x, ga.y);
-          dk[2 * k4 + 1] = pack_bf16x2(gb.x, gb.y);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = h * 4 + u;
-          *reinterpret_cast<uint4*>(dsrow + ((c ^ (r & 7)) * 16)) =
-              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(BAR(B_DSREADY));
-        mbar_arrive(BAR(B_STEMPTY + st));  // this tile's LSE/D are no longer read
-      }
-    }
-    if (ok) {
-      const bool w = mbar_wait(BAR(B_ACC), 0, a.status, a.wait_limit_ns);
-      ok = __all_sync(0xffffffffu, w);
-    }
-    if (!ok) {
-      *abort_flag = 1;
-    } else {
-      // epilogue: group 0 writes dV, group 1 writes dK (which carries the
-      // softmax scale of dS); a query range of a split unit leaves its fp32
-      // partial sums (dK unscaled) for the dQ-convert stage to add up
-      tc_fence_after();
-      if (tail_unit >= 0) {
-        float* prow = a.dKVpart + ((size_t)(tail_unit * a.splits + part) * 2 + g) * (size_t)C::BK * D +
-                      (size_t)r * D;
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + (g == 0 ? C::COL_DV : C::COL_DK) + 32 * q, v);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[32];
+          tmem_ld32(lane_addr + C::COL_S + 64 * g + 32 * h, sr);
           tmem_ld_wait();
-          if (key_live) {
-            float4* d4 = reinterpret_cast<float4*>(prow + 32 * q);
+          uint32_t pk[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                  __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          for (int k4 = 0; k4 < 8; ++k4) {
+            // nl = -LSE*log2e of four query columns
+            const float4 nl = *reinterpret_cast<const float4*>(lse2 + 32 * h + 4 * k4);
+            const float2 xa = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4]), __uint_as_float(sr[4 * k4 + 1])), c22, f2_pack(nl.x, nl.y)));
+            const float2 xb = f2_unpack(ffma2(f2_pack(__uint_as_float(sr[4 * k4 + 2]), __uint_as_float(sr[4 * k4 + 3])), c22, f2_pack(nl.z, nl.w)));
+            float p0 = ex2_approx(xa.x), p1 = ex2_approx(xa.y), p2 = ex2_approx(xb.x), p3 = ex2_approx(xb.y);
+            if (!key_live) p0 = p1 = p2 = p3 = 0.f;
+            if (diag) {
+              const int c = 32 * h + 4 * k4;
+              p0 = c < r_rel ? 0.f : p0;
+              p1 = c + 1 < r_rel ? 0.f : p1;
+              p2 = c + 2 < r_rel ? 0.f : p2;
+              p3 = c + 3 < r_rel ? 0.f : p3;
+            }
+            pf[16 * h + 2 * k4] = f2_pack(p0, p1);
+            pf[16 * h + 2 * k4 + 1] = f2_pack(p2, p3);
+            pk[2 * k4] = pack_bf16x2(p0, p1);
+            pk[2 * k4 + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st16(lane_addr + C::COL_S + 64 * g + 16 * h, pk);
+        }
+        // P^T of this group's 64 queries goes to the first 32 of its own S^T
+        // columns (64g .. 64g+31), so neither group overwrites scores the
+        // other has not read yet; the dV products take their A slices there.
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_PTREADY));
+        // phase 2: dS'^T = P^T o (dP^T - D), bf16, into this group's swizzled
+        // [128 keys][64 queries] chunk of the dS^T tile (16-byte unit c of row r
+        // lands at unit c ^ (r & 7))
+        w_ok = mbar_wait(BAR(B_DPFULL), gt & 1, a.status, a.wait_limit_ns) &&
+               mbar_wait(BAR(B_DSEMPTY), (gt & 1) ^ 1, a.status, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t dr[32];
+          tmem_ld32(lane_addr + C::COL_DP + 64 * g + 32 * h, dr);
+          tmem_ld_wait();
+          uint32_t dk[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            // nd = -D of four query columns; dS' = P * (dP - D). The softmax
+            // scale of dS is applied once to dK (epilogue) and dQ (convert).
+            const float4 nd = *reinterpret_cast<const float4*>(drow + 32 * h + 4 * k4);
+            const uint64_t ta = fadd2(f2_pack(__uint_as_float(dr[4 * k4]), __uint_as_float(dr[4 * k4 + 1])), f2_pack(nd.x, nd.y));
+            const uint64_t tb = fadd2(f2_pack(__uint_as_float(dr[4 * k4 + 2]), __uint_as_float(dr[4 * k4 + 3])), f2_pack(nd.z, nd.w));
+            const float2 ga = f2_unpack(fmul2(pf[16 * h + 2 * k4], ta));
+            const float2 gb = f2_unpack(fmul2(pf[16 * h + 2 * k4 + 1], tb));
+            dk[2 * k4] = pack_bf16x2(ga.x, ga.y);
+            dk[2 * k4 + 1] = pack_bf16x2(gb.x, gb.y);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = h * 4 + u;
+            *reinterpret_cast<uint4*>(dsrow + ((c ^ (r & 7)) * 16)) =
+                make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
           }
         }
-      } else {
-      const size_t out_row = key_live ? seq_row_offset(a.seq, sv, k0 + r) : 0;
-      const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
-      const float f = g == 0 ? 1.f : scale;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK) + out_row;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(BAR(B_DSREADY));
+          mbar_arrive(BAR(B_STEMPTY + st));  // this tile's LSE/D are no longer read
+        }
+      }
+      if (!ok) break;
+      if constexpr (!C::EPI_DQ) {
+        // epilogue: group 0 writes dV, group 1 writes dK (which carries the
+        // softmax scale of dS); a query range of a split unit leaves its fp32
+        // partial sums (dK unscaled) for the dQ-convert stage to add up. The
+        // next item's first dV (dK) product overwrites these columns only
+        // after this warp's next pt_ready (ds_ready) arrival.
+        {
+          const bool w_ok = mbar_wait(BAR(B_ACC), ui & 1, a.status, a.wait_limit_ns);
+          if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
+        }
+        tc_fence_after();
+        BwdItem it;  // decoded again: keeps the tile loop's registers free
+        bwd_item<C::BK, C::BQ>(a, list, w, it);
+        const int k0 = it.kb * C::BK;
+        const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
+        if (it.tail_unit >= 0) {
+          float* prow = a.dKVpart + ((size_t)(it.tail_unit * a.splits + it.part) * 2 + g) * (size_t)C::BK * D +
+                        (size_t)r * D;
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + col + 32 * q, v);
+            tmem_ld_wait();
+            if (key_live) {
+              float4* d4 = reinterpret_cast<float4*>(prow + 32 * q);
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        uint32_t v[32];
-        tmem_ld32(lane_addr + col + 32 * q, v);
-        tmem_ld_wait();
-        if (key_live) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * q);
+              for (int u = 0; u < 8; ++u)
+                d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+            }
+          }
+        } else {
+          // The warp stages its 32 rows, 64 columns (128 bytes of bf16) at a
+          // time, in its own rows of the group's dS^T chunk (free here: the
+          // item's dK and dQ products, its readers, are complete, and the
+          // group writes it again only in its next phase 2), in the 128-byte
+          // swizzle, and reads them back so that each store instruction
+          // writes 4 whole 128-byte rows instead of 16 bytes of 32 rows.
+          const float f = g == 0 ? 1.f : a.scale;
+          __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK);
+          uint8_t* stg = smem + C::OFF_DS + g * C::ROW_CHUNK + wq * 32 * 128;  // [32 rows][128 B]
+          const int rsub = lane >> 3, unit = lane & 7;  // read-back: row 4j + rsub, 16-byte unit
+#pragma unroll 1
+          for (int hc = 0; hc < D / 64; ++hc) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            d4[u] = make_uint4(pack_bf16x2(f * __uint_as_float(v[8 * u]), f * __uint_as_float(v[8 * u + 1])),
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t v[32];
+              tmem_ld32(lane_addr + col + 64 * hc + 32 * hh, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(dsrow + (((4 * hh + u) ^ (lane & 7)) << 4)) =
+                    make_uint4(pack_bf16x2(f * __uint_as_float(v[8 * u]), f * __uint_as_float(v[8 * u + 1])),
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 2]), f * __uint_as_float(v[8 * u + 3])),
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int rr = 4 * j + rsub;  // row within the warp's 32
+              const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((unit ^ (rr & 7)) << 4));
+              const int key = k0 + wq * 32 + rr;
+              if (key < it.sv.len)
+                *reinterpret_cast<uint4*>(base + seq_row_offset(a.seq, it.sv, key) + 64 * hc + 8 * unit) = x;
+            }
+            __syncwarp();  // the rows are read before the next pass (or phase 2) writes them
+          }
         }
       }
-      }
+      ++ui;
+      g0 += n_it;
     }
+    if (!ok) *abort_flag = 1;
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ reduction
     const int wq = warp & 3;  // TMEM lanes 32wq..32wq+31: d indices (dQ^T) or query rows (dQ)
@@ -707,72 +849,169 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     constexpr int HALF = NCOL / 2;             // read in two halves (register budget)
     uint8_t* wstage = smem + C::OFF_DQS + wq * 2 * C::DQ_BLOCK_BYTES;
     int nblk = 0;  // staging blocks issued so far by this warp
-    for (int i = 0; i < n_it; ++i) {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const bool w = mbar_wait(BAR(B_DQFULL), i & 1, a.status, a.wait_limit_ns);
-      if (!__all_sync(0xffffffffu, w)) { *abort_flag = 1; break; }
-      tc_fence_after();
-      // rows past the sequence receive exact zeros (their P is 0)
-      const size_t row0 = ws_row0 + (size_t)(i_begin + i) * C::BQ;
+    int ui = 0, g0 = 0;  // items and query tiles before this item
+    bool ok = true;
+    for (int w = w_first; ok && w < w_end; w += w_step) {
+      size_t row_first;  // workspace row of the item's first query tile
+      int n_it;
+      {
+        BwdItem it;
+        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        row_first = (size_t)it.sv.plane * a.ws_rows + (size_t)it.sv.start + (size_t)it.i_begin * C::BQ;
+        n_it = it.n_it;
+      }
+      for (int i = 0; i < n_it; ++i) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+        const bool w_ok = mbar_wait(BAR(B_DQFULL), (g0 + i) & 1, a.status, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, w_ok)) { *abort_flag = 1; ok = false; break; }
+        tc_fence_after();
+        // rows past the sequence receive exact zeros (their P is 0)
+        const size_t row0 = row_first + (size_t)i * C::BQ;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t v[HALF];
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[HALF];
 #pragma unroll
-        for (int q = 0; q < HALF / 32; ++q)
-          tmem_ld32(lane_addr + C::COL_DP + HALF * hh + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * q]));
-        tmem_ld_wait();
-        if (hh == 1) {
-          // all of dQ(i) is in registers: the MMA warp may reuse the columns
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_DQEMPTY));
-        }
-        if (C::DQ_T) {
-          // lane t holds dQ[row0 + q][t] for this half's queries. Each warp
-          // stages its 32 d-columns of 32 query rows at a time ([row][32 d]
-          // fp32, 4 KB) and lets the TMA engine add the block into the
-          // accumulator; two buffers per warp, tracked by the warp's lane 0.
+          for (int q = 0; q < HALF / 32; ++q)
+            tmem_ld32(lane_addr + C::COL_DP + HALF * hh + 32 * q, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * q]));
+          tmem_ld_wait();
+          if (hh == 1) {
+            // all of dQ(i) is in registers: the MMA warp may reuse the columns
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(B_DQEMPTY));
+          }
+          if (C::DQ_T) {
+            // lane t holds dQ[row0 + q][t] for this half's queries. Each warp
+            // stages its 32 d-columns of 32 query rows at a time ([row][32 d]
+            // fp32, 4 KB) and lets the TMA engine add the block into the
+            // accumulator; two buffers per warp, tracked by the warp's lane 0.
 #pragma unroll
-          for (int c = 0; c < HALF / C::DQ_ROWS; ++c, ++nblk) {
+            for (int c = 0; c < HALF / C::DQ_ROWS; ++c, ++nblk) {
+              const int buf = nblk & 1;
+              if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
+              __syncwarp();
+              float* stage = reinterpret_cast<float*>(wstage + buf * C::DQ_BLOCK_BYTES);
+#pragma unroll
+              for (int q = 0; q < C::DQ_ROWS; ++q) stage[q * 32 + lane] = __uint_as_float(v[C::DQ_ROWS * c + q]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), wq * 32,
+                                  (int)(row0 + (size_t)HALF * hh + (size_t)C::DQ_ROWS * c));
+                bulk_commit_group();
+              }
+            }
+          } else {
+            // lane t holds this half (32 columns) of the dQ row of query
+            // row0 + t. The warp stages its 32 rows x 32 columns as [row][32]
+            // fp32 in the TMA 128-byte swizzle (16-byte unit k of row r at unit
+            // k ^ (r % 8): the float4 stores of the 32 lanes hit every bank
+            // equally) and lets the TMA engine add the block into the
+            // accumulator; two buffers per warp, tracked by the warp's lane 0.
             const int buf = nblk & 1;
             if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
             __syncwarp();
-            float* stage = reinterpret_cast<float*>(wstage + buf * C::DQ_BLOCK_BYTES);
+            uint8_t* stage = wstage + buf * C::DQ_BLOCK_BYTES;
 #pragma unroll
-            for (int q = 0; q < C::DQ_ROWS; ++q) stage[q * 32 + lane] = __uint_as_float(v[C::DQ_ROWS * c + q]);
+            for (int k = 0; k < HALF / 4; ++k)
+              *reinterpret_cast<float4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                  make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                              __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), wq * 32,
-                                (int)(row0 + (size_t)HALF * hh + (size_t)C::DQ_ROWS * c));
+              tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), HALF * hh, (int)(row0 + (size_t)wq * 32));
               bulk_commit_group();
             }
+            ++nblk;
           }
-        } else {
-          // lane t holds this half (32 columns) of the dQ row of query
-          // row0 + t. The warp stages its 32 rows x 32 columns as [row][32]
-          // fp32 in the TMA 128-byte swizzle (16-byte unit k of row r at unit
-          // k ^ (r % 8): the float4 stores of the 32 lanes hit every bank
-          // equally) and lets the TMA engine add the block into the
-          // accumulator; two buffers per warp, tracked by the warp's lane 0.
-          const int buf = nblk & 1;
-          if (lane == 0) bulk_wait_group_read<1>();  // the reduction that last read buf is done
-          __syncwarp();
-          uint8_t* stage = wstage + buf * C::DQ_BLOCK_BYTES;
-#pragma unroll
-          for (int k = 0; k < HALF / 4; ++k)
-            *reinterpret_cast<float4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-                make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                            __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_reduce_add_2d(&a.tmDQacc, smem_u32(stage), HALF * hh, (int)(row0 + (size_t)wq * 32));
-            bulk_commit_group();
-          }
-          ++nblk;
         }
       }
+      if (!ok) break;
+      if constexpr (C::EPI_DQ) {
+      // epilogue of the item: dV, then dK (which carries the softmax scale
+      // of dS), one key row per thread (TMEM lane 32wq + lane); a query
+      // range of a split unit leaves its fp32 partial sums (dK unscaled) for
+      // the dQ-convert stage to add up
+      {
+        const bool w_ok = mbar_wait(BAR(B_ACC), ui & 1, a.status, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, w_ok)) { *abort_flag = 1; ok = false; break; }
+      }
+      tc_fence_after();
+      BwdItem it;  // decoded again: keeps the tile loop's registers free
+      bwd_item<C::BK, C::BQ>(a, list, w, it);
+      const int r = wq * 32 + lane;
+      const int k0 = it.kb * C::BK;
+      if (it.tail_unit >= 0) {
+        const bool key_live = k0 + r < it.sv.len;
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          float* prow = a.dKVpart + ((size_t)(it.tail_unit * a.splits + it.part) * 2 + g) * (size_t)C::BK * D +
+                        (size_t)r * D;
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + (g == 0 ? C::COL_DV : C::COL_DK) + 32 * q, v);
+            tmem_ld_wait();
+            if (key_live) {
+              float4* d4 = reinterpret_cast<float4*>(prow + 32 * q);
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                d4[u] = make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+            }
+          }
+        }
+      } else {
+        // The warp stages its 32 rows, 64 columns (128 bytes of bf16) at a
+        // time, in its dQ staging buffer (free once its reductions have read
+        // it) in the 128-byte swizzle, and reads them back so that each store
+        // instruction writes 4 whole 128-byte rows instead of 16 bytes of 32
+        // rows.
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        uint8_t* stg = wstage;  // [32 rows][128 B]
+        const int rsub = lane >> 3, unit = lane & 7;  // read-back: row 4j + rsub, 16-byte unit
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
+          const float f = g == 0 ? 1.f : a.scale;
+          __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK);
+#pragma unroll 1
+          for (int hc = 0; hc < D / 64; ++hc) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t v[32];
+              tmem_ld32(lane_addr + col + 64 * hc + 32 * hh, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(stg + lane * 128 + (((4 * hh + u) ^ (lane & 7)) << 4)) =
+                    make_uint4(pack_bf16x2(f * __uint_as_float(v[8 * u]), f * __uint_as_float(v[8 * u + 1])),
+                               pack_bf16x2(f * __uint_as_float(v[8 * u + 2]), f * __uint_as_float(v[8 * u + 3])),
+                               pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
+                               pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int rr = 4 * j + rsub;  // row within the warp's 32
+              const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((unit ^ (rr & 7)) << 4));
+              const int key = k0 + wq * 32 + rr;
+              if (key < it.sv.len)
+                *reinterpret_cast<uint4*>(base + seq_row_offset(a.seq, it.sv, key) + 64 * hc + 8 * unit) = x;
+            }
+            __syncwarp();  // the rows are read before the next pass writes them
+          }
+        }
+      }
+      // dV and dK have left TMEM: the next item may overwrite them
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_ACCEMPTY));
+      }
+      ++ui;
+      g0 += n_it;
     }
     // every bulk reduction must have read its staging block before the CTA
     // exits; the additions land before the kernel ends
@@ -806,11 +1045,18 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
     if (e != cudaSuccess) return e;
     const unsigned kblocks = (unsigned)((a.seq.N + C::BK - 1) / C::BK);
     dim3 grid(kblocks, (unsigned)BH);
-    if (a.splits > 1) {
-      if (a.seq.causal || a.seq.cu_seqlens || a.dKVpart == nullptr || a.n_tail < 1 ||
-          (long long)a.n_full + a.n_tail != (long long)kblocks * BH)
+    if (a.items > 0) {
+      // persistent grid over the item list: one CTA per SM (each holds all of
+      // TMEM and most of shared memory)
+      if (a.seq.causal || a.seq.cu_seqlens || a.splits < 1 || a.n_tail < 0 ||
+          (long long)a.n_full + a.n_tail != (long long)kblocks * BH ||
+          (long long)a.items != (long long)a.n_full + (long long)a.n_tail * a.splits ||
+          (a.splits > 1 && (a.dKVpart == nullptr || a.n_tail < 1)))
         return cudaErrorInvalidValue;
-      grid = dim3((unsigned)((long long)a.n_full + (long long)a.n_tail * a.splits));
+      const int sms = fwd_slots();
+      grid = dim3((unsigned)(sms > 0 && sms < a.items ? sms : a.items));
+    } else if (a.splits > 1) {
+      return cudaErrorInvalidValue;  // a split tail runs only as an item list
     } else if (a.seq.causal) {
       // every CTA of a head streams the head's Q and dO and adds into its dQ accumulator
       const int hpg = causal_heads_per_group(BH, 8ll * a.seq.N * D, 48ll << 20);

@@ -382,6 +382,7 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.n_tail = L.plan.n_tail;
   a.splits = L.plan.splits;
   a.dKVpart = L.plan.splits > 1 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
+  a.items = (sq.causal || sq.cu_seqlens) ? 0 : L.plan.n_full + L.plan.n_tail * L.plan.splits;
   return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -119,11 +119,15 @@ struct BwdArgs {
   int debug_skip_q;
   // Tail split (fixed length, non-causal, splits > 1): units (batch*head,
   // 128-key tile), key tile fastest, 0..n_full-1 run whole; the n_tail units
-  // after them run as `splits` ranges of query tiles each, one CTA per range,
+  // after them run as `splits` ranges of query tiles each, one item per range,
   // leaving fp32 partial dV and dK (unscaled) in dKVpart; the dQ-convert
-  // stage adds the ranges up. splits = 1: the usual 2-D grids.
+  // stage adds the ranges up. splits = 1: every unit runs whole.
   int n_full, n_tail, splits;
   float* dKVpart;  // fp32 [n_tail][splits][2 (dV, dK)][128][d]
+  // Items of the main kernel's persistent grid (fixed length, non-causal):
+  // n_full + n_tail * splits, walked by min(items, SM count) CTAs with
+  // stride gridDim.x. 0: one unit per CTA of the 2-D/3-D grids.
+  int items;
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
 // The backward's tail split for `units` (batch*head, key tile) units with n_q

@@ -159,9 +159,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt);
 
 /*
  * The schedule of the bf16 backward's main kernel for this problem (no GPU
- * work). It runs one CTA per (batch*head, 128-key tile) unit, one CTA per SM;
- * when the last wave fills at most half of the SMs, its *n_tail units run as
- * *splits ranges of query tiles each, one CTA per range, and the dQ-convert
+ * work). Its work items are (batch*head, 128-key tile) units, walked by a
+ * persistent grid of one CTA per SM (item w by CTA w mod W, in order);
+ * when the last round of items fills at most half of the SMs, its *n_tail
+ * units run as *splits ranges of query tiles each, one item per range, and the dQ-convert
  * stage adds their partial dK and dV up ("Lesson 1: FlashAttention core
  * idea" §5: dK_j and dV_j are sums over the query tiles). *n_full units run
  * whole (*splits = 1, *n_tail = 0: nothing split). The rule, with W CTAs at
@@ -349,7 +350,9 @@ fa_status fa_debug_timeout_probe(long long limit_ns, void* stream);
  * mask), plus:
  *   skip_tile  the forward's producer skips the load of key tile `skip_tile`
  *              of every CTA; the backward's producer skips the Q tile of
- *              query iteration `skip_tile` of every CTA. Neither the copy nor
+ *              query iteration `skip_tile` of every CTA (a CTA of the
+ *              persistent grid counts its iterations over all the units it
+ *              walks, in order). Neither the copy nor
  *              its expected-bytes arrival is issued, so no copy is left in
  *              flight; the consumers' bounded waits on that tile run out.
  *              Must be in [1, ceil(N / 128) - 1], else FA_ERR_INVALID_ARG.

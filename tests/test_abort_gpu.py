@@ -62,8 +62,9 @@ def test_forward_skipped_key_tile_times_out_then_recovers(d, H):
 
 @pytest.mark.parametrize("d,H,N", [(128, 2, 768), (64, 2, 768), (128, 10, 2000)])
 def test_backward_skipped_query_tile_times_out_then_recovers(d, H, N):
-    """H = 2, N = 768: 6 query tiles per CTA, 12 CTAs. H = 10, N = 2000: 160 units,
-    the last 8 split into query ranges (every range CTA skips its third tile)."""
+    """H = 2, N = 768: 6 query tiles per unit, 12 units, one per CTA. H = 10,
+    N = 2000: 160 units, the last 8 split into query ranges, so 32 CTAs walk a
+    whole unit and then a range (each CTA skips the third tile of its walk)."""
     lib = fa.load_library()
     B = 1
     q, k, v, do = (t.cuda() for t in random_qkv(B, H, N, d, torch.bfloat16, seed=51 + d))
