@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   const int sub = lane / LPR, l = lane % LPR;
   const long long prow = (long long)warp_global * RPW + sub;  // workspace row index
   const long long total = (long long)a.planes * a.ws_rows;
+  if (blockIdx.x == 0 && threadIdx.x == 0 && a.item_counter != nullptr) *a.item_counter = 0;  // the main kernel's item counter
   float acc = 0.f;
   bool live = false;
   long long plane = 0, n = 0;
@@ -221,9 +222,12 @@ struct BwdCfg {
   static_assert(OFF_DQS % 1024 == 0, "swizzled staging alignment");
   // barriers: kv_full, q_full[QS], q_empty[QS], do_full[DS], do_empty[DS], st_full[2],
   //           st_empty[2], s_full, dp_full, pt_ready, ds_ready, ds_empty, dq_full,
-  //           dq_empty, acc_done, drain, kv_empty, acc_empty
-  static constexpr int NBAR = 1 + 2 * QSTAGES + 2 * DOSTAGES + 2 * STATSTAGES + 11;
-  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
+  //           dq_empty, acc_done, drain, kv_empty, acc_empty, item_full[IRING],
+  //           item_empty[IRING]
+  static constexpr int IRING = 4;  // items published ahead by the producer
+  static constexpr int NBAR = 1 + 2 * QSTAGES + 2 * DOSTAGES + 2 * STATSTAGES + 11 + 2 * IRING;
+  // after the barriers: TMEM base, abort flag, 8 bytes free, the item ring
+  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 4 * IRING;
   static constexpr int SMEM_MAX = 227 * 1024;
   // request 1 KB of alignment slack when it fits; the kernel checks alignment
   static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 <= SMEM_MAX) ? SMEM_BYTES + 1024 : SMEM_MAX;
@@ -251,11 +255,12 @@ struct BwdItem {
   int part;       // query range of a split unit
 };
 
-// Item w of the 1-D item list (fixed length, non-causal: units key tile
-// fastest, those from n_full on as `splits` query ranges each), or, with
-// list == false, this CTA's unit of the 2-D/3-D grids (variable length,
-// causal). False: nothing to do (a head past the last one, a key tile past
-// the sequence's end). Out of line: every role decodes each of its items, and
+// Item w of the 1-D item list of a fixed-length problem (non-causal: units
+// key tile fastest, those from n_full on as `splits` query ranges each;
+// causal: head groups, then key tiles in increasing order, then the heads of
+// the group), or, with list == false, this CTA's unit of the 2-D/3-D grids
+// (packed batches). False: nothing to do (a head past the last one, a key
+// tile past the sequence's end). Out of line: every role decodes each of its items, and
 // one shared copy keeps the kernel's code (and instruction-cache footprint)
 // small.
 template <int BK, int BQ>
@@ -264,7 +269,15 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
   int bh;
   it.tail_unit = -1;
   it.part = 0;
-  if (list) {
+  if (w < 0) return false;
+  if (list && causal) {
+    // (heads of a group, key tiles in increasing order = most query tiles
+    // first, head groups): the order of the one-CTA-per-unit causal grid
+    const int kblocks = (a.seq.N + BK - 1) / BK;
+    const int x = w % a.causal_hpg, rest = w / a.causal_hpg;
+    it.kb = rest % kblocks;
+    bh = (rest / kblocks) * a.causal_hpg + x;
+  } else if (list) {
     const int kblocks = (a.seq.N + BK - 1) / BK;
     int u = w;
     if (u >= a.n_full) {
@@ -299,16 +312,24 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
   return it.n_it > 0;
 }
 
-// Fixed-length, non-causal problems run as a persistent grid (a.items > 0):
-// one CTA per SM walks the item list with stride gridDim.x, so the set-up,
-// the TMEM allocation and the CTA turnaround are paid once per SM, and the
-// next item's first loads and products overlap this item's last tile and
-// epilogue. Every role walks the same items; the rings and the per-tile
-// barriers continue across items (global tile index g), the K/V tile and the
-// dV/dK accumulators are handed over per item (kv_empty; the next item's
-// first dV and dK products come after the softmax warps' epilogue, which
-// precedes their next pt_ready and ds_ready arrivals).
-template <int D>
+// Fixed-length problems run as a persistent grid (a.items > 0; causal ones
+// up to 32 key tiles): one CTA per SM takes items from the list, its first
+// one by block index and, non-causal (items of one length), every gridDim.x-th
+// after it; causal, each next one from a device counter (zeroed by the
+// preprocess), so the SMs take the items, longest first, as they become free.
+// The set-up, the TMEM allocation and the CTA turnaround are paid once per SM,
+// and the next item's first loads and products overlap this item's last
+// tile and epilogue. The producer takes each item and publishes it to the
+// other roles through a small ring in shared memory; the rings and the
+// per-tile barriers continue across items (global tile index g), the K/V
+// tile and the dV/dK accumulators are handed over per item (kv_empty; the
+// next item's first dV and dK products come after the epilogue: acc_empty
+// from the dQ warps, or the softmax warps' next pt_ready and ds_ready
+// arrivals).
+// DYN: the causal item list, taken from the counter through the item ring;
+// otherwise every role steps through the items itself (list: by stride
+// gridDim.x; grid: its one unit), and no ring or counter code is compiled in.
+template <int D, bool DYN>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -329,18 +350,17 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             B_DPFULL = B_SFULL + 1, B_PTREADY = B_SFULL + 2, B_DSREADY = B_SFULL + 3,
             B_DSEMPTY = B_SFULL + 4, B_DQFULL = B_SFULL + 5, B_DQEMPTY = B_SFULL + 6,
             B_ACC = B_SFULL + 7, B_DRAIN = B_SFULL + 8, B_KVEMPTY = B_SFULL + 9,
-            B_ACCEMPTY = B_SFULL + 10;
+            B_ACCEMPTY = B_SFULL + 10, B_ITF = B_SFULL + 11, B_ITE = B_ITF + C::IRING;
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 16);
   const float* stat_smem = reinterpret_cast<const float*>(smem + C::OFF_STAT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
   const bool list = a.items > 0;
-  const int w_first = list ? (int)blockIdx.x : 0;
-  const int w_step = list ? (int)gridDim.x : 1;
-  const int w_end = list ? a.items : 1;
-  if (w_first >= w_end) return;
+  const int n_items = list ? a.items : 1;  // item indices >= n_items end the walk
+  if (list && (int)blockIdx.x >= n_items) return;
   if (!list) {
     BwdItem it0;
     if (!bwd_item<C::BK, C::BQ>(a, false, 0, it0)) return;  // no key of a sequence here
@@ -371,6 +391,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_KVEMPTY), 1);
     mbar_init(BAR(B_ACCEMPTY), 4);  // one arrival per dQ warp, after its epilogue
+    for (int s = 0; s < C::IRING; ++s) {
+      mbar_init(BAR(B_ITF + s), 1);   // the producer
+      mbar_init(BAR(B_ITE + s), 14);  // one arrival per consuming warp: MMA, statistics, 8 softmax, 4 dQ
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -379,6 +403,24 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // n-th item of this CTA for a consuming warp (warp-uniform). DYN: the
+  // index the producer published (false, abort raised, if it never comes);
+  // otherwise the n-th of the CTA's stride.
+  auto next_item = [&](int n, int& w) {
+    if constexpr (DYN) {
+      const int slot = n % C::IRING;
+      if (!mbar_wait_warp(BAR(B_ITF + slot), (n / C::IRING) & 1, a.status, a.wait_limit_ns)) {
+        if (lane == 0) *abort_flag = 1;
+        return false;
+      }
+      w = item_ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_ITE + slot));
+    } else {
+      w = list ? (int)blockIdx.x + n * (int)gridDim.x : n;
+    }
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer: K, V, Q ring
@@ -391,9 +433,35 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       for (int s = 0; s < C::QSTAGES; ++s) last[s] = -1;
       int ui = 0, g0 = 0;  // items and query tiles before this item
       bool ok = true;
-      for (int w = w_first; ok && w < w_end; w += w_step) {
+      int w = list ? (int)blockIdx.x : 0;
+      for (int n = 0; ok; ++n) {
+        if constexpr (DYN) {
+          // publish the item (or the end of the walk) to the other roles
+          const int slot = n % C::IRING;
+          if (n >= C::IRING &&
+              !mbar_wait(BAR(B_ITE + slot), ((n / C::IRING) - 1) & 1, a.status, a.wait_limit_ns)) {
+            ok = false;
+            break;
+          }
+          item_ring[slot] = w;
+          mbar_arrive(BAR(B_ITF + slot));
+        }
+        if (w >= n_items) break;
+        // the item after this one, taken now so that its K and V can be
+        // prefetched while this one runs: causal items (of decreasing
+        // length) from the counter, the others (all of one length) by stride
+        int w_next = n_items;
+        if constexpr (DYN) {
+          const int c = atomicAdd(a.item_counter, 1);
+          w_next = c >= 0 && c < n_items ? (int)gridDim.x + c : n_items;
+        } else {
+          if (list) w_next = w + (int)gridDim.x;
+        }
         BwdItem it;
-        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) {
+          w = w_next;
+          continue;
+        }
         const int plane = it.sv.plane, qrow0 = it.sv.start + it.i_begin * C::BQ;
         auto load_q = [&](int i) {  // query tile i_begin + i into its ring slot
           const int g = g0 + i;
@@ -427,6 +495,17 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         ++ui;
         for (; ok && i < it.n_it; ++i) ok = *abort_flag == 0 && load_q(i);
         g0 += it.n_it;
+        if (ok && w_next < n_items) {
+          // the next item's K and V into L2 now, a few tiles before this
+          // item's last dQ releases the buffer they load into
+          BwdItem nx;
+          if (bwd_item<C::BK, C::BQ>(a, list, w_next, nx))
+            for (int c = 0; c < C::CH; ++c) {
+              tma_prefetch_l2_3d(&a.tmK, c * 64, nx.sv.start + nx.kb * C::BK, nx.sv.plane);
+              tma_prefetch_l2_3d(&a.tmV, c * 64, nx.sv.start + nx.kb * C::BK, nx.sv.plane);
+            }
+        }
+        w = w_next;
       }
       if (!ok) *abort_flag = 1;
       // drain: the last load issued into each buffer must have landed before exit
@@ -450,7 +529,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     int last_stat = -1;  // lane 0: last statistics tile issued by bulk copies
     int g0 = 0;
     bool ok = true;
-    for (int w = w_first; ok && w < w_end; w += w_step) {
+    for (int n = 0; ok; ++n) {
+      int w;
+      if (!next_item(n, w)) { ok = false; break; }
+      if (w >= n_items) break;
       BwdItem it;
       if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
       const int N = it.sv.len, plane = it.sv.plane;
@@ -580,7 +662,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       };
       bool ok = true;
       int ui = 0, g0 = 0;  // items and query tiles before this item
-      for (int w = w_first; ok && w < w_end; w += w_step) {
+      for (int n = 0; ok; ++n) {
+        int w;
+        if (!next_item(n, w)) { ok = false; break; }
+        if (w >= n_items) break;
         BwdItem it;
         if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
         const int n_it = it.n_it;
@@ -661,7 +746,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     uint8_t* dsrow = smem + C::OFF_DS + g * C::ROW_CHUNK + r * 128;  // this group's dS^T chunk
     bool ok = true;
     int ui = 0, g0 = 0;  // items and query tiles before this item
-    for (int w = w_first; ok && w < w_end; w += w_step) {
+    for (int n = 0; ok; ++n) {
+      int w;
+      if (!next_item(n, w)) { ok = false; break; }
+      if (w >= n_items) break;
       int n_it, diag_i;
       bool key_live;
       {
@@ -803,8 +891,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           // time, in its own rows of the group's dS^T chunk (free here: the
           // item's dK and dQ products, its readers, are complete, and the
           // group writes it again only in its next phase 2), in the 128-byte
-          // swizzle, and reads them back so that each store instruction
-          // writes 4 whole 128-byte rows instead of 16 bytes of 32 rows.
+          // swizzle. Fixed length: one TMA tensor store of the 32 x 64 box
+          // (rows past N are clipped); packed batches read the rows back so
+          // that each store instruction writes 4 whole 128-byte rows of this
+          // sequence instead of 16 bytes of 32 rows.
+          const bool tma_out = a.seq.cu_seqlens == nullptr;
           const float f = g == 0 ? 1.f : a.scale;
           __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK);
           uint8_t* stg = smem + C::OFF_DS + g * C::ROW_CHUNK + wq * 32 * 128;  // [32 rows][128 B]
@@ -824,16 +915,28 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
             }
-            __syncwarp();
+            if (tma_out) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(g == 0 ? &a.tmdV : &a.tmdK, smem_u32(stg), 64 * hc, it.sv.start + k0 + wq * 32,
+                             it.sv.plane);
+                bulk_commit_group();
+                bulk_wait_group_read<0>();  // the rows are read before the next pass (or phase 2) writes them
+              }
+              __syncwarp();
+            } else {
+              __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int rr = 4 * j + rsub;  // row within the warp's 32
-              const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((unit ^ (rr & 7)) << 4));
-              const int key = k0 + wq * 32 + rr;
-              if (key < it.sv.len)
-                *reinterpret_cast<uint4*>(base + seq_row_offset(a.seq, it.sv, key) + 64 * hc + 8 * unit) = x;
+              for (int j = 0; j < 8; ++j) {
+                const int rr = 4 * j + rsub;  // row within the warp's 32
+                const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((unit ^ (rr & 7)) << 4));
+                const int key = k0 + wq * 32 + rr;
+                if (key < it.sv.len)
+                  *reinterpret_cast<uint4*>(base + seq_row_offset(a.seq, it.sv, key) + 64 * hc + 8 * unit) = x;
+              }
+              __syncwarp();  // the rows are read before the next pass (or phase 2) writes them
             }
-            __syncwarp();  // the rows are read before the next pass (or phase 2) writes them
           }
         }
       }
@@ -841,6 +944,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       g0 += n_it;
     }
     if (!ok) *abort_flag = 1;
+    if (lane == 0) bulk_wait_group_all();  // the epilogue's tensor stores have completed
   } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ reduction
     const int wq = warp & 3;  // TMEM lanes 32wq..32wq+31: d indices (dQ^T) or query rows (dQ)
@@ -851,7 +955,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     int nblk = 0;  // staging blocks issued so far by this warp
     int ui = 0, g0 = 0;  // items and query tiles before this item
     bool ok = true;
-    for (int w = w_first; ok && w < w_end; w += w_step) {
+    for (int n = 0; ok; ++n) {
+      int w;
+      if (!next_item(n, w)) { ok = false; break; }
+      if (w >= n_items) break;
       size_t row_first;  // workspace row of the item's first query tile
       int n_it;
       {
@@ -964,16 +1071,19 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
       } else {
         // The warp stages its 32 rows, 64 columns (128 bytes of bf16) at a
-        // time, in its dQ staging buffer (free once its reductions have read
-        // it) in the 128-byte swizzle, and reads them back so that each store
-        // instruction writes 4 whole 128-byte rows instead of 16 bytes of 32
-        // rows.
+        // time, in its dQ staging buffers (free once its reductions have read
+        // them; dV in the first, dK in the second) in the 128-byte swizzle.
+        // Fixed length: one TMA tensor store per 32 x 64 box (rows past N
+        // are clipped); packed batches read the rows back so that each store
+        // instruction writes 4 whole 128-byte rows of this sequence instead
+        // of 16 bytes of 32 rows.
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
-        uint8_t* stg = wstage;  // [32 rows][128 B]
+        const bool tma_out = a.seq.cu_seqlens == nullptr;
         const int rsub = lane >> 3, unit = lane & 7;  // read-back: row 4j + rsub, 16-byte unit
 #pragma unroll 1
         for (int g = 0; g < 2; ++g) {
+          uint8_t* stg = wstage + g * C::DQ_BLOCK_BYTES;  // [32 rows][128 B]
           const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
           const float f = g == 0 ? 1.f : a.scale;
           __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(g == 0 ? a.dV : a.dK);
@@ -992,18 +1102,33 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 4]), f * __uint_as_float(v[8 * u + 5])),
                                pack_bf16x2(f * __uint_as_float(v[8 * u + 6]), f * __uint_as_float(v[8 * u + 7])));
             }
-            __syncwarp();
+            if (tma_out) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(g == 0 ? &a.tmdV : &a.tmdK, smem_u32(stg), 64 * hc, it.sv.start + k0 + wq * 32,
+                             it.sv.plane);
+                bulk_commit_group();
+                if (hc + 1 < D / 64) bulk_wait_group_read<0>();  // the buffer takes the next pass
+              }
+              __syncwarp();
+            } else {
+              __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int rr = 4 * j + rsub;  // row within the warp's 32
-              const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((unit ^ (rr & 7)) << 4));
-              const int key = k0 + wq * 32 + rr;
-              if (key < it.sv.len)
-                *reinterpret_cast<uint4*>(base + seq_row_offset(a.seq, it.sv, key) + 64 * hc + 8 * unit) = x;
+              for (int j = 0; j < 8; ++j) {
+                const int rr = 4 * j + rsub;  // row within the warp's 32
+                const uint4 x = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((unit ^ (rr & 7)) << 4));
+                const int key = k0 + wq * 32 + rr;
+                if (key < it.sv.len)
+                  *reinterpret_cast<uint4*>(base + seq_row_offset(a.seq, it.sv, key) + 64 * hc + 8 * unit) = x;
+              }
+              __syncwarp();  // the rows are read before the next pass writes them
             }
-            __syncwarp();  // the rows are read before the next pass writes them
           }
         }
+        // the staging buffers take dQ blocks again only after these stores read them
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
       }
       // dV and dK have left TMEM: the next item may overwrite them
       tc_fence_before();
@@ -1040,19 +1165,26 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
     if (e != cudaSuccess) return e;
   }
   if (stages & kStageMain) {
-    e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_ALLOC);
+    const bool dyn = a.items > 0 && a.seq.causal;
+    e = cudaFuncSetAttribute(dyn ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const unsigned kblocks = (unsigned)((a.seq.N + C::BK - 1) / C::BK);
     dim3 grid(kblocks, (unsigned)BH);
     if (a.items > 0) {
       // persistent grid over the item list: one CTA per SM (each holds all of
       // TMEM and most of shared memory)
-      if (a.seq.causal || a.seq.cu_seqlens || a.splits < 1 || a.n_tail < 0 ||
-          (long long)a.n_full + a.n_tail != (long long)kblocks * BH ||
-          (long long)a.items != (long long)a.n_full + (long long)a.n_tail * a.splits ||
-          (a.splits > 1 && (a.dKVpart == nullptr || a.n_tail < 1)))
+      if (a.seq.cu_seqlens || a.item_counter == nullptr) return cudaErrorInvalidValue;
+      if (a.seq.causal) {
+        const int hpg = causal_heads_per_group(BH, 8ll * a.seq.N * D, 48ll << 20);
+        if (a.splits != 1 || a.causal_hpg != hpg ||
+            (long long)a.items != (long long)hpg * kblocks * ((BH + hpg - 1) / hpg))
+          return cudaErrorInvalidValue;
+      } else if (a.splits < 1 || a.n_tail < 0 || (long long)a.n_full + a.n_tail != (long long)kblocks * BH ||
+                 (long long)a.items != (long long)a.n_full + (long long)a.n_tail * a.splits ||
+                 (a.splits > 1 && (a.dKVpart == nullptr || a.n_tail < 1))) {
         return cudaErrorInvalidValue;
+      }
       const int sms = fwd_slots();
       grid = dim3((unsigned)(sms > 0 && sms < a.items ? sms : a.items));
     } else if (a.splits > 1) {
@@ -1062,7 +1194,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
       const int hpg = causal_heads_per_group(BH, 8ll * a.seq.N * D, 48ll << 20);
       grid = dim3((unsigned)hpg, kblocks, (unsigned)((BH + hpg - 1) / hpg));
     }
-    bwd_main_kernel<D><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
+    if (dyn) bwd_main_kernel<D, true><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
+    else bwd_main_kernel<D, false><<<grid, C::THREADS, C::SMEM_ALLOC, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -157,14 +157,14 @@ SeqArgs varlen_seq(const int* cu_seqlens, int H, int total, int max_seqlen, int 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct BwdWorkspaceLayout {
-  size_t dqacc, lse2, drow, part, total;
+  size_t dqacc, lse2, drow, part, sched, total;
   int planes, ws_rows;
   BwdTailPlan plan;
 };
 // fp32: D per row ([planes, total]). bf16: fp32 dQ accumulator
 // [planes, ws_rows, d], two per-row statistics [planes, ws_rows] and, when the
 // schedule splits its tail (fixed length, non-causal, on the current device),
-// the split units' fp32 partial dV and dK.
+// the split units' fp32 partial dV and dK, and the main kernel's item counter.
 BwdWorkspaceLayout bwd_layout(const SeqArgs& sq, int B, int d, fa_dtype dt) {
   BwdWorkspaceLayout L{};
   L.plan = BwdTailPlan{0, 0, 1};
@@ -183,7 +183,8 @@ BwdWorkspaceLayout bwd_layout(const SeqArgs& sq, int B, int d, fa_dtype dt) {
   L.part = L.drow + align_up(P * L.ws_rows * sizeof(float), 256);
   if (!sq.causal && sq.cu_seqlens == nullptr)
     L.plan = plan_bwd_tail((long long)B * sq.H * ((sq.N + 127) / 128), (sq.N + 127) / 128, fwd_slots());
-  L.total = L.part + bwd_tail_part_bytes(L.plan, d);
+  L.sched = L.part + bwd_tail_part_bytes(L.plan, d);
+  L.total = L.sched + 256;
   return L;
 }
 
@@ -356,7 +357,9 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   if (!encode_seq_bf16(&a.tmQ, Q, sq, L.planes, d, qrows) ||
       !encode_seq_bf16(&a.tmK, K, sq, L.planes, d, 128) ||
       !encode_seq_bf16(&a.tmV, V, sq, L.planes, d, 128) ||
-      !encode_seq_bf16(&a.tmdO, dO, sq, L.planes, d, qrows))
+      !encode_seq_bf16(&a.tmdO, dO, sq, L.planes, d, qrows) ||
+      !encode_seq_bf16(&a.tmdK, dK, sq, L.planes, d, 32) ||
+      !encode_seq_bf16(&a.tmdV, dV, sq, L.planes, d, 32))
     return FA_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   a.O = O;
@@ -382,7 +385,19 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.n_tail = L.plan.n_tail;
   a.splits = L.plan.splits;
   a.dKVpart = L.plan.splits > 1 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
-  a.items = (sq.causal || sq.cu_seqlens) ? 0 : L.plan.n_full + L.plan.n_tail * L.plan.splits;
+  a.item_counter = reinterpret_cast<int*>(ws + L.sched);
+  if (sq.cu_seqlens == nullptr && !(sq.causal && sq.N > 32 * 128)) {
+    // fixed length: the persistent grid's item list (longer causal sequences
+    // keep one CTA per unit: their units are long enough that the set-up is
+    // a small share, and the hardware's block dispatch balances them best)
+    const int kblocks = (sq.N + 127) / 128;
+    if (sq.causal) {
+      a.causal_hpg = causal_heads_per_group(BH, 8ll * sq.N * d, 48ll << 20);
+      a.items = a.causal_hpg * kblocks * ((BH + a.causal_hpg - 1) / a.causal_hpg);
+    } else {
+      a.items = L.plan.n_full + L.plan.n_tail * L.plan.splits;
+    }
+  }
   return launch_bwd_bf16(a, BH, d, stages, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

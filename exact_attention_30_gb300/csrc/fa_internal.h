@@ -94,6 +94,7 @@ int fwd_slots();
 
 struct BwdArgs {
   CUtensorMap tmQ, tmK, tmV, tmdO;  // 3-D (d, rows, planes) views of the SeqArgs layout
+  CUtensorMap tmdK, tmdV;           // the same views of dK, dV; 32-row boxes (epilogue stores)
   CUtensorMap tmDQacc;  // fp32 [planes*ws_rows, d], 32 x 32 boxes; 128-byte swizzle at d = 64
   const void* O;     // bf16, SeqArgs layout (as Q, K, V, dO, dQ, dK, dV)
   const void* dO;
@@ -124,10 +125,15 @@ struct BwdArgs {
   // stage adds the ranges up. splits = 1: every unit runs whole.
   int n_full, n_tail, splits;
   float* dKVpart;  // fp32 [n_tail][splits][2 (dV, dK)][128][d]
-  // Items of the main kernel's persistent grid (fixed length, non-causal):
-  // n_full + n_tail * splits, walked by min(items, SM count) CTAs with
-  // stride gridDim.x. 0: one unit per CTA of the 2-D/3-D grids.
+  // Items of the main kernel's persistent grid (fixed length): non-causal
+  // n_full + n_tail * splits, taken by min(items, SM count) CTAs with stride
+  // gridDim.x; causal (up to 32 key tiles) causal_hpg * key tiles * head
+  // groups (heads past BH skipped), the first by block index, the rest from
+  // *item_counter (zeroed by the preprocess stage). 0: one unit per CTA of
+  // the 2-D/3-D grids (packed batches, longer causal sequences).
   int items;
+  int causal_hpg;     // heads per group of the causal item order
+  int* item_counter;  // in the workspace
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
 // The backward's tail split for `units` (batch*head, key tile) units with n_q

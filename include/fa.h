@@ -197,12 +197,15 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * separately. Same arguments and validation as fa_bwd, plus `stage`:
  *   FA_BWD_PREPROCESS (0): per-row statistics from D = rowsum(dO o O) and
  *                          the LSE into the workspace; zero the workspace's
- *                          dQ accumulator.
+ *                          dQ accumulator and (bf16) the main stage's unit
+ *                          counter.
  *   FA_BWD_MAIN       (1): recompute P tile by tile; write dK, dV (the
  *                          split units of fa_bwd_plan: partial sums into the
  *                          workspace); add dQ into the workspace accumulator
  *                          (for bf16 without the softmax scale). Needs stage
- *                          0 done.
+ *                          0 done since the last main stage on this
+ *                          workspace (a causal bf16 problem of up to 4096
+ *                          keys takes its units from that counter).
  *   FA_BWD_DQ_CONVERT (2): workspace dQ accumulator -> dQ in dtype `dt`
  *                          (bf16: the scale is applied here), and the split
  *                          units' partial dK, dV added up into dK, dV.

@@ -1,11 +1,14 @@
-"""GPU parity of the bf16 backward's persistent grid: fixed-length, non-causal
-problems run as one CTA per SM walking the (batch*head, key tile) items, so a
-CTA carries its rings, barriers and tensor memory from one item to the next.
+"""GPU parity of the bf16 backward's persistent grid: fixed-length problems
+run as one CTA per SM taking (batch*head, key tile) items in list order from
+a device counter, so a CTA carries its rings, barriers and tensor memory from
+one item to the next.
 
 Checks, against the fp64 oracle with the bf16 gradient bar, EVERY head of
-problems where each CTA walks several items: ragged key and query tiles,
-whole items followed by the query ranges of a split tail, and short items of
-one query tile. A second run gives the same dK and dV bits.
+problems where each CTA takes several items: ragged key and query tiles,
+whole items followed by the query ranges of a split tail, short items of one
+query tile, and causal items of decreasing length. A second run gives the
+same dK and dV bits (each item's dK and dV come from one CTA whatever the
+order the items are taken in).
 """
 import math
 
@@ -26,27 +29,32 @@ def _items(B, H, N, d):
     return n_full + n_tail * splits
 
 
-@pytest.mark.parametrize("B,H,N,d", [
-    (3, 67, 300, 64),     # 603 items of 3 query tiles, ragged last key and query tiles
-    (1, 40, 1000, 128),   # 320 units: 304 whole, then 16 split into query ranges
-    (2, 90, 128, 128),    # 180 items of a single query tile
-    (4, 40, 520, 64),     # 800 items of 5 tiles, 8 rows in the last
+@pytest.mark.parametrize("B,H,N,d,causal", [
+    (3, 67, 300, 64, False),    # 603 items of 3 query tiles, ragged last key and query tiles
+    (1, 40, 1000, 128, False),  # 320 units: 304 whole, then 16 split into query ranges
+    (2, 90, 128, 128, False),   # 180 items of a single query tile
+    (4, 40, 520, 64, False),    # 800 items of 5 tiles, 8 rows in the last
+    (3, 67, 300, 64, True),     # causal: 603 items of 3, 2 and 1 query tiles, longest first
+    (1, 40, 1000, 128, True),   # causal: 320 items of 8 down to 1 query tile
+    (2, 30, 2048, 64, True),    # causal: head groups, items of 16 down to 1 tile
 ])
-def test_persistent_backward_every_head(B, H, N, d):
+def test_persistent_backward_every_head(B, H, N, d, causal):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert _items(B, H, N, d) > sms  # some CTA walks more than one item
-    q, k, v, do = random_qkv(B, H, N, d, torch.bfloat16, seed=B * H + N + d)
+    assert B * H * -(-N // 128) > sms  # some CTA walks more than one item
+    if not causal:
+        assert _items(B, H, N, d) > sms
+    q, k, v, do = random_qkv(B, H, N, d, torch.bfloat16, seed=B * H + N + d + int(causal))
     qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     scale = 1 / math.sqrt(d)
-    o, lse = fa.fa_fwd(qc, kc, vc, scale)
-    grads = fa.fa_bwd(qc, kc, vc, o, doc, lse, scale)
+    o, lse = fa.fa_fwd(qc, kc, vc, scale, causal=causal)
+    grads = fa.fa_bwd(qc, kc, vc, o, doc, lse, scale, causal=causal)
     torch.cuda.synchronize()
     assert fa.fa_check_device_status() == fa.FA_OK
     q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
     g64 = [to64(g) for g in grads]
     for b in range(B):
         for h in range(H):
-            ref = attention_bwd(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale)
+            ref = attention_bwd(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale, causal=causal)
             cancel = float(np.abs(do64[b, h]).max() * np.abs(v64[b, h]).max() * d)
             for name, got, r in zip(("dQ", "dK", "dV"), g64, ref):
                 assert grad_within(got[b, h], r, cancel), (name, b, h, rel_max(got[b, h], r))
