@@ -187,11 +187,6 @@ struct BwdCfg {
   // dQ = dS K (queries on the lanes; an M = 64 product would be needed
   // otherwise) and stages each lane's row through a swizzled block
   static constexpr bool DQ_T = (D == 128);
-  // Who writes an item's dV and dK: at d = 64 the dQ warps (lightly loaded
-  // there; the softmax warps go straight on to the next item), at d = 128
-  // the softmax warps (the dQ warps' read-out of 128 columns per tile is on
-  // the critical loop). Both measured; each is the faster one at its d.
-  static constexpr bool EPI_DQ = (D == 64);
   static constexpr int CH = D / 64;                  // 128-byte chunks per K/V/Q/dO row
   // Q_i (with its LSE/D statistics) is read by S^T(i), issued one tile
   // early, and last by dK(i); dO_i by dP^T(i), also issued one tile early,
@@ -332,6 +327,11 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
 template <int D, bool DYN>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
+  // Who writes an item's dV and dK: the dQ warps (the softmax warps go
+  // straight on to the next item), except in the causal-list kernel at
+  // d = 128, where the softmax warps do (there the dQ warps' register budget
+  // spills). Measured both ways; each is the faster one where it is used.
+  constexpr bool EPI_DQ = (D == 64) || !DYN;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           // the first dV (and dK) product of a later item overwrites the
           // accumulators once the dQ warps have written the previous item's
           // (softmax-warp epilogue: their pt_ready arrivals follow it)
-          if (C::EPI_DQ && i == 0 && ui > 0 && !wait(B_ACCEMPTY, (ui - 1) & 1)) { ok = false; break; }
+          if (EPI_DQ && i == 0 && ui > 0 && !wait(B_ACCEMPTY, (ui - 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_dv(so, i > 0);
           mma_commit(BAR(B_DOEMPTY + so), leader);  // dO_i: last use was dV
@@ -855,7 +855,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
       }
       if (!ok) break;
-      if constexpr (!C::EPI_DQ) {
+      if constexpr (!EPI_DQ) {
         // epilogue: group 0 writes dV, group 1 writes dK (which carries the
         // softmax scale of dS); a query range of a split unit leaves its fp32
         // partial sums (dK unscaled) for the dQ-convert stage to add up. The
@@ -1035,7 +1035,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
       }
       if (!ok) break;
-      if constexpr (C::EPI_DQ) {
+      if constexpr (EPI_DQ) {
       // epilogue of the item: dV, then dK (which carries the softmax scale
       // of dS), one key row per thread (TMEM lane 32wq + lane); a query
       // range of a split unit leaves its fp32 partial sums (dK unscaled) for
