@@ -152,15 +152,17 @@ fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, fl
  * Bytes of device scratch that fa_bwd needs for this problem on the CURRENT
  * device (0 on invalid arguments). The caller allocates it; its contents on
  * entry do not matter. Holds the fp32 dQ accumulator, per-row statistics
- * derived from D = rowsum(dO o O) and the LSE and, when the schedule splits
- * its tail (fa_bwd_plan), the split units' fp32 partial dK and dV.
+ * derived from D = rowsum(dO o O) and the LSE, the main kernel's unit
+ * counter and, when the schedule splits its tail (fa_bwd_plan), the split
+ * units' fp32 partial dK and dV.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d, fa_dtype dt);
 
 /*
  * The schedule of the bf16 backward's main kernel for this problem (no GPU
- * work). Its work items are (batch*head, 128-key tile) units, walked by a
- * persistent grid of one CTA per SM (item w by CTA w mod W, in order);
+ * work). Its work items are (batch*head, 128-key tile) units, taken by a
+ * persistent grid of one CTA per SM (non-causal: item w by CTA w mod W, in
+ * order);
  * when the last round of items fills at most half of the SMs, its *n_tail
  * units run as *splits ranges of query tiles each, one item per range, and the dQ-convert
  * stage adds their partial dK and dV up ("Lesson 1: FlashAttention core
