@@ -558,7 +558,7 @@ def run_gpu(args):
                    "flops_per_step": STEP_FLOPS,
                    "l2": "flushed before every step (256 MiB write, outside the per-step events)",
                    "parallelism": f"replicas x{world}, independent batches, no collective"},
-        "roofline": {"kernel": f"bwd_main_kernel<{D}, {'true' if causal and N <= 4096 else 'false'}>",
+        "roofline": {"kernel": f"bwd_main_kernel<{D}, {'true' if causal else 'false'}>",
                      "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": peak_label,

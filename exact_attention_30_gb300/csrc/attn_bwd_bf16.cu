@@ -307,11 +307,11 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
   return it.n_it > 0;
 }
 
-// Fixed-length problems run as a persistent grid (a.items > 0; causal ones
-// up to 32 key tiles): one CTA per SM takes items from the list, its first
-// one by block index and, non-causal (items of one length), every gridDim.x-th
-// after it; causal, each next one from a device counter (zeroed by the
-// preprocess), so the SMs take the items, longest first, as they become free.
+// Fixed-length problems run as a persistent grid (a.items > 0): one CTA per
+// SM takes items from the list, its first one by block index and,
+// non-causal (items of one length), every gridDim.x-th after it; causal,
+// each next one from a device counter (zeroed by the preprocess), so the SMs
+// take the items, longest first, as they become free.
 // The set-up, the TMEM allocation and the CTA turnaround are paid once per SM,
 // and the next item's first loads and products overlap this item's last
 // tile and epilogue. The producer takes each item and publishes it to the
@@ -447,19 +447,24 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           mbar_arrive(BAR(B_ITF + slot));
         }
         if (w >= n_items) break;
-        // the item after this one, taken now so that its K and V can be
-        // prefetched while this one runs: causal items (of decreasing
-        // length) from the counter, the others (all of one length) by stride
-        int w_next = n_items;
-        if constexpr (DYN) {
-          const int c = atomicAdd(a.item_counter, 1);
-          w_next = c >= 0 && c < n_items ? (int)gridDim.x + c : n_items;
-        } else {
-          if (list) w_next = w + (int)gridDim.x;
-        }
+        // The item after this one: causal items (of decreasing length) from
+        // the counter, taken once this item's last Q load is issued (a few
+        // tiles before it ends: an earlier claim would hold a long item's
+        // successor back while other SMs run dry); the others (all of one
+        // length) by stride.
+        auto take_next = [&]() {
+          int wn = n_items;
+          if constexpr (DYN) {
+            const int c = atomicAdd(a.item_counter, 1);
+            wn = c >= 0 && c < n_items ? (int)gridDim.x + c : n_items;
+          } else {
+            if (list) wn = w + (int)gridDim.x;
+          }
+          return wn;
+        };
         BwdItem it;
         if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) {
-          w = w_next;
+          w = take_next();
           continue;
         }
         const int plane = it.sv.plane, qrow0 = it.sv.start + it.i_begin * C::BQ;
@@ -495,6 +500,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         ++ui;
         for (; ok && i < it.n_it; ++i) ok = *abort_flag == 0 && load_q(i);
         g0 += it.n_it;
+        const int w_next = take_next();
         if (ok && w_next < n_items) {
           // the next item's K and V into L2 now, a few tiles before this
           // item's last dQ releases the buffer they load into

@@ -386,10 +386,8 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.splits = L.plan.splits;
   a.dKVpart = L.plan.splits > 1 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
   a.item_counter = reinterpret_cast<int*>(ws + L.sched);
-  if (sq.cu_seqlens == nullptr && !(sq.causal && sq.N > 32 * 128)) {
-    // fixed length: the persistent grid's item list (longer causal sequences
-    // keep one CTA per unit: their units are long enough that the set-up is
-    // a small share, and the hardware's block dispatch balances them best)
+  if (sq.cu_seqlens == nullptr) {
+    // fixed length: the persistent grid's item list
     const int kblocks = (sq.N + 127) / 128;
     if (sq.causal) {
       a.causal_hpg = causal_heads_per_group(BH, 8ll * sq.N * d, 48ll << 20);

@@ -127,10 +127,10 @@ struct BwdArgs {
   float* dKVpart;  // fp32 [n_tail][splits][2 (dV, dK)][128][d]
   // Items of the main kernel's persistent grid (fixed length): non-causal
   // n_full + n_tail * splits, taken by min(items, SM count) CTAs with stride
-  // gridDim.x; causal (up to 32 key tiles) causal_hpg * key tiles * head
-  // groups (heads past BH skipped), the first by block index, the rest from
-  // *item_counter (zeroed by the preprocess stage). 0: one unit per CTA of
-  // the 2-D/3-D grids (packed batches, longer causal sequences).
+  // gridDim.x; causal causal_hpg * key tiles * head groups (heads past BH
+  // skipped), the first by block index, the rest from *item_counter (zeroed
+  // by the preprocess stage). 0: one unit per CTA of the 2-D grid (packed
+  // batches).
   int items;
   int causal_hpg;     // heads per group of the causal item order
   int* item_counter;  // in the workspace

@@ -206,8 +206,8 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  *                          workspace); add dQ into the workspace accumulator
  *                          (for bf16 without the softmax scale). Needs stage
  *                          0 done since the last main stage on this
- *                          workspace (a causal bf16 problem of up to 4096
- *                          keys takes its units from that counter).
+ *                          workspace (a causal bf16 problem takes its units
+ *                          from that counter).
  *   FA_BWD_DQ_CONVERT (2): workspace dQ accumulator -> dQ in dtype `dt`
  *                          (bf16: the scale is applied here), and the split
  *                          units' partial dK, dV added up into dK, dV.

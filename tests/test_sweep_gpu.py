@@ -3,8 +3,8 @@
 Shapes are drawn (seeded) so that, between them, they reach every schedule
 the library picks: one unit per CTA and several per CTA (the backward's
 persistent grid), split last rounds (forward key ranges, backward query
-ranges), causal item lists whose last head group is padded, causal grids
-past 4096 keys, the four-tile d = 64 forward, and ragged last tiles. Each
+ranges), causal item lists whose last head group is padded, more than 32
+key tiles, the four-tile d = 64 forward, and ragged last tiles. Each
 case checks O, LSE, dQ, dK and dV of three heads (first, last, one drawn)
 with the bars of the other bf16 tests.
 """
@@ -30,7 +30,7 @@ def _cases():
         causal = (i // 2) % 2 == 1
         N = int(rng.integers(1, 3000))
         if i % 8 == 7:
-            N = int(rng.integers(4097, 5200))  # causal past 4096 keys: one CTA per unit
+            N = int(rng.integers(4097, 5200))  # more than 32 key tiles
         BH = int(rng.integers(1, 64)) if N > 1000 else int(rng.integers(1, 300))
         H = int(rng.integers(1, 9))
         B = max(1, BH // H)
