@@ -15,9 +15,9 @@
 //                P = 0 there), and zero the fp32 dQ accumulator.
 //  2. bwd_main:  per unit (batch*head, 128-key tile j): K_j, V_j stay in
 //                shared memory while 128-query tiles i stream through a TMA
-//                ring. Fixed-length, non-causal problems run a persistent
-//                grid (one CTA per SM walking the units); causal and packed
-//                batches one CTA per unit. All products run on tcgen05 with fp32 accumulators in
+//                ring. A persistent grid (one CTA per SM) takes the units:
+//                by stride when they have one length, else longest first
+//                from a device counter (causal, packed batches). All products run on tcgen05 with fp32 accumulators in
 //                TMEM (every MMA M = N = 128):
 //                  S^T = K_j Q_i^T,  dP^T = V_j dO_i^T   (recompute; keys on lanes)
 //                  dV += P^T dO_i (P^T read from TMEM), dK += dS^T Q_i
@@ -61,8 +61,69 @@ namespace {
 // One group of D/8 lanes per row; each lane reads 8 bf16 of O and dO.
 // Rows of whole planes: plane p, row n < ws_rows; rows n < total are data
 // (of whichever sequence holds them), the rest padding.
+// Packed batches: the main kernel's item list, longest sequence first. One
+// block of the preprocess launch: each sequence's length (0 for an invalid
+// pair of offsets), its rank by length (descending, then index; index order
+// past 1024 sequences), and per rank the prefix sum of its units (H * key
+// tiles): schedule ints [0] the item counter (zeroed), [1] the item total,
+// [2 ..] the order, then the B + 1 prefix sums.
+template <int BK>
+__device__ void bwd_sched_block(const BwdArgs& a) {
+  int* sched = a.item_counter;
+  const int B = a.nseq, H = a.seq.H;
+  int* order = sched + 2;
+  int* prefix = order + B;
+  __shared__ int lens[1024];
+  __shared__ int part[256];
+  const int t = threadIdx.x;
+  auto len_of = [&](int b) {
+    const int c0 = a.seq.cu_seqlens[b], c1 = a.seq.cu_seqlens[b + 1];
+    return (0 <= c0 && c0 <= c1 && c1 <= a.seq.total && c1 - c0 <= a.seq.N) ? c1 - c0 : 0;
+  };
+  if (B <= 1024) {
+    for (int b = t; b < B; b += 256) lens[b] = len_of(b);
+    __syncthreads();
+    for (int b = t; b < B; b += 256) {
+      const int lb = lens[b];
+      int r = 0;
+      for (int b2 = 0; b2 < B; ++b2) r += (lens[b2] > lb) || (lens[b2] == lb && b2 < b);
+      order[r] = b;
+    }
+  } else {
+    for (int b = t; b < B; b += 256) order[b] = b;
+  }
+  __syncthreads();  // order[] (global, this block's writes) visible to the block
+  const int per = (B + 255) / 256;
+  const int r0 = min(B, t * per), r1 = min(B, r0 + per);
+  int sum = 0;
+  for (int r = r0; r < r1; ++r) sum += H * ((len_of(order[r]) + BK - 1) / BK);
+  part[t] = sum;
+  __syncthreads();
+  if (t == 0) {
+    int acc = 0;
+    for (int i = 0; i < 256; ++i) {
+      const int v = part[i];
+      part[i] = acc;
+      acc += v;
+    }
+    sched[0] = 0;
+    sched[1] = acc;
+    prefix[B] = acc;
+  }
+  __syncthreads();
+  int acc = part[t];
+  for (int r = r0; r < r1; ++r) {
+    prefix[r] = acc;
+    acc += H * ((len_of(order[r]) + BK - 1) / BK);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  if (a.nseq > 0 && blockIdx.x == gridDim.x - 1) {  // the extra block: the packed batch's schedule
+    bwd_sched_block<128>(a);
+    return;
+  }
   constexpr int LPR = D / 8;            // lanes per row
   constexpr int RPW = 32 / LPR;         // rows per warp
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -222,7 +283,8 @@ struct BwdCfg {
   static constexpr int IRING = 4;  // items published ahead by the producer
   static constexpr int NBAR = 1 + 2 * QSTAGES + 2 * DOSTAGES + 2 * STATSTAGES + 11 + 2 * IRING;
   // after the barriers: TMEM base, abort flag, 8 bytes free, the item ring
-  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 4 * IRING;
+  // (IRING published items, 8 ints each)
+  static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 32 * IRING;
   static constexpr int SMEM_MAX = 227 * 1024;
   // request 1 KB of alignment slack when it fits; the kernel checks alignment
   static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 <= SMEM_MAX) ? SMEM_BYTES + 1024 : SMEM_MAX;
@@ -265,7 +327,26 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
   it.tail_unit = -1;
   it.part = 0;
   if (w < 0) return false;
-  if (list && causal) {
+  if (list && a.seq.cu_seqlens != nullptr) {
+    // packed batch: sequences longest first (the preprocess's order), then
+    // heads, then key tiles; the rank by binary search of the unit prefix
+    const int* order = a.item_counter + 2;
+    const int* prefix = order + a.nseq;
+    int lo = 0, hi = a.nseq;  // prefix[lo] <= w < prefix[hi]
+    if (w >= prefix[hi]) return false;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= w) lo = mid;
+      else hi = mid;
+    }
+    const int b = order[lo], local = w - prefix[lo];
+    const int c0 = a.seq.cu_seqlens[b], c1 = a.seq.cu_seqlens[b + 1];
+    const int kblocks = (c1 - c0 + BK - 1) / BK;  // >= 1 (the rank has units)
+    if (kblocks < 1) return false;
+    const int h = local / kblocks;
+    it.kb = local - h * kblocks;
+    bh = b * a.seq.H + h;
+  } else if (list && causal) {
     // (heads of a group, key tiles in increasing order = most query tiles
     // first, head groups): the order of the one-CTA-per-unit causal grid
     const int kblocks = (a.seq.N + BK - 1) / BK;
@@ -307,11 +388,12 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
   return it.n_it > 0;
 }
 
-// Fixed-length problems run as a persistent grid (a.items > 0): one CTA per
-// SM takes items from the list, its first one by block index and,
-// non-causal (items of one length), every gridDim.x-th after it; causal,
-// each next one from a device counter (zeroed by the preprocess), so the SMs
-// take the items, longest first, as they become free.
+// The main kernel runs as a persistent grid (a.items > 0): one CTA per SM
+// takes items from the list, its first one by block index and, fixed-length
+// non-causal (items of one length), every gridDim.x-th after it; causal and
+// packed batches, each next one from a device counter (zeroed by the
+// preprocess), so the SMs take the items, longest first, as they become
+// free.
 // The set-up, the TMEM allocation and the CTA turnaround are paid once per SM,
 // and the next item's first loads and products overlap this item's last
 // tile and epilogue. The producer takes each item and publishes it to the
@@ -321,9 +403,10 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
 // next item's first dV and dK products come after the epilogue: acc_empty
 // from the dQ warps, or the softmax warps' next pt_ready and ds_ready
 // arrivals).
-// DYN: the causal item list, taken from the counter through the item ring;
-// otherwise every role steps through the items itself (list: by stride
-// gridDim.x; grid: its one unit), and no ring or counter code is compiled in.
+// DYN: the causal and packed-batch item lists, taken from the counter and
+// published decoded through the item ring; otherwise every role steps
+// through the items itself (list: by stride gridDim.x; grid: its one unit),
+// and no ring or counter code is compiled in.
 template <int D, bool DYN>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
@@ -354,12 +437,26 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 4);
   volatile int* item_ring = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + C::NBAR * 8 + 16);
+  auto ring_item = [&](int slot) {
+    const volatile int* p = item_ring + 8 * slot;
+    BwdItem it;
+    it.sv.plane = p[0];
+    it.sv.start = p[1];
+    it.sv.len = p[2];
+    it.kb = p[3];
+    it.i_begin = p[4];
+    it.n_it = p[5];
+    it.tail_unit = p[6];
+    it.part = p[7];
+    return it;
+  };
   const float* stat_smem = reinterpret_cast<const float*>(smem + C::OFF_STAT);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool causal = a.seq.causal != 0;
   const bool list = a.items > 0;
-  const int n_items = list ? a.items : 1;  // item indices >= n_items end the walk
+  // item indices >= n_items end the walk (a packed batch's total is in its schedule)
+  const int n_items = !list ? 1 : (a.seq.cu_seqlens != nullptr ? a.item_counter[1] : a.items);
   if (list && (int)blockIdx.x >= n_items) return;
   if (!list) {
     BwdItem it0;
@@ -403,23 +500,38 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // n-th item of this CTA for a consuming warp (warp-uniform). DYN: the
-  // index the producer published (false, abort raised, if it never comes);
-  // otherwise the n-th of the CTA's stride.
-  auto next_item = [&](int n, int& w) {
+  // The n-th item of this CTA for a consuming warp (warp-uniform), into
+  // `it`: 0 an item, 1 the end of the walk, 2 nothing here (skip), -1 the wait
+  // ran out (abort raised). DYN: the item the producer decoded and published
+  // (its slot is held until release_item(n)); otherwise the n-th of the
+  // CTA's stride, decoded here.
+  auto get_item = [&](int n, BwdItem& it) -> int {
     if constexpr (DYN) {
       const int slot = n % C::IRING;
       if (!mbar_wait_warp(BAR(B_ITF + slot), (n / C::IRING) & 1, a.status, a.wait_limit_ns)) {
         if (lane == 0) *abort_flag = 1;
-        return false;
+        return -1;
       }
-      w = item_ring[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_ITE + slot));
+      it = ring_item(slot);
+      return it.n_it == 0 ? 1 : 0;
     } else {
-      w = list ? (int)blockIdx.x + n * (int)gridDim.x : n;
+      const int w = list ? (int)blockIdx.x + n * (int)gridDim.x : n;
+      if (w >= n_items) return 1;
+      return bwd_item<C::BK, C::BQ>(a, list, w, it) ? 0 : 2;
     }
-    return true;
+  };
+  // The n-th item again (the epilogues read it again: that keeps the tile
+  // loops' registers free).
+  auto reload_item = [&](int n, BwdItem& it) {
+    if constexpr (DYN) it = ring_item(n % C::IRING);
+    else bwd_item<C::BK, C::BQ>(a, list, list ? (int)blockIdx.x + n * (int)gridDim.x : n, it);
+  };
+  // DYN: this warp is done with the n-th item's ring slot.
+  auto release_item = [&](int n) {
+    if constexpr (DYN) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_ITE + n % C::IRING));
+    }
   };
 
   if (warp == 0) {
@@ -434,39 +546,51 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       int ui = 0, g0 = 0;  // items and query tiles before this item
       bool ok = true;
       int w = list ? (int)blockIdx.x : 0;
-      for (int n = 0; ok; ++n) {
+      // The item after this one: DYN (items of different lengths: causal,
+      // packed batches) from the counter, taken once this item's last Q load
+      // is issued (a few tiles before it ends: an earlier claim would hold a
+      // long item's successor back while other SMs run dry); the others (all
+      // of one length) by stride.
+      auto take_next = [&]() {
+        int wn = n_items;
         if constexpr (DYN) {
-          // publish the item (or the end of the walk) to the other roles
+          const int c = atomicAdd(a.item_counter, 1);
+          wn = c >= 0 && c < n_items ? (int)gridDim.x + c : n_items;
+        } else {
+          if (list) wn = w + (int)gridDim.x;
+        }
+        return wn;
+      };
+      for (int n = 0; ok; ++n) {
+        // the item, past any with nothing to do (heads padding the last
+        // causal head group)
+        BwdItem it;
+        bool end = false;
+        for (;;) {
+          if (w >= n_items) { end = true; break; }
+          if (bwd_item<C::BK, C::BQ>(a, list, w, it)) break;
+          w = take_next();
+        }
+        if constexpr (DYN) {
+          // publish the decoded item (n_it = 0: the end of the walk)
           const int slot = n % C::IRING;
           if (n >= C::IRING &&
               !mbar_wait(BAR(B_ITE + slot), ((n / C::IRING) - 1) & 1, a.status, a.wait_limit_ns)) {
             ok = false;
             break;
           }
-          item_ring[slot] = w;
+          volatile int* p = item_ring + 8 * slot;
+          p[0] = it.sv.plane;
+          p[1] = it.sv.start;
+          p[2] = it.sv.len;
+          p[3] = it.kb;
+          p[4] = it.i_begin;
+          p[5] = end ? 0 : it.n_it;
+          p[6] = it.tail_unit;
+          p[7] = it.part;
           mbar_arrive(BAR(B_ITF + slot));
         }
-        if (w >= n_items) break;
-        // The item after this one: causal items (of decreasing length) from
-        // the counter, taken once this item's last Q load is issued (a few
-        // tiles before it ends: an earlier claim would hold a long item's
-        // successor back while other SMs run dry); the others (all of one
-        // length) by stride.
-        auto take_next = [&]() {
-          int wn = n_items;
-          if constexpr (DYN) {
-            const int c = atomicAdd(a.item_counter, 1);
-            wn = c >= 0 && c < n_items ? (int)gridDim.x + c : n_items;
-          } else {
-            if (list) wn = w + (int)gridDim.x;
-          }
-          return wn;
-        };
-        BwdItem it;
-        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) {
-          w = take_next();
-          continue;
-        }
+        if (end) break;
         const int plane = it.sv.plane, qrow0 = it.sv.start + it.i_begin * C::BQ;
         auto load_q = [&](int i) {  // query tile i_begin + i into its ring slot
           const int g = g0 + i;
@@ -536,11 +660,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     int g0 = 0;
     bool ok = true;
     for (int n = 0; ok; ++n) {
-      int w;
-      if (!next_item(n, w)) { ok = false; break; }
-      if (w >= n_items) break;
       BwdItem it;
-      if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+      const int got = get_item(n, it);
+      if (got < 0) { ok = false; break; }
+      if (got == 1) break;
+      if (got == 2) continue;
       const int N = it.sv.len, plane = it.sv.plane;
       const size_t ws_row0 = (size_t)plane * a.ws_rows + (size_t)it.sv.start;  // workspace row of query 0
       for (int i = 0; i < it.n_it; ++i) {
@@ -594,7 +718,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
         __syncwarp();
       }
+      if (!ok) break;
       g0 += it.n_it;
+      release_item(n);
     }
     if (lane == 0) {
       // the last dO and statistics copies issued into each slot must have
@@ -669,11 +795,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       bool ok = true;
       int ui = 0, g0 = 0;  // items and query tiles before this item
       for (int n = 0; ok; ++n) {
-        int w;
-        if (!next_item(n, w)) { ok = false; break; }
-        if (w >= n_items) break;
         BwdItem it;
-        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        const int got = get_item(n, it);
+        if (got < 0) { ok = false; break; }
+        if (got == 1) break;
+        if (got == 2) continue;
         const int n_it = it.n_it;
         {
           // the item's first S^T and dP^T (S^T overwrites P^T of the previous
@@ -734,6 +860,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         mma_commit(BAR(B_ACC), leader);  // the item's dV and dK are complete
         g0 += n_it;
         ++ui;
+        release_item(n);
       }
       if (!ok && lane == 0) *abort_flag = 1;
       mma_commit(BAR(B_DRAIN), leader);
@@ -753,14 +880,14 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     bool ok = true;
     int ui = 0, g0 = 0;  // items and query tiles before this item
     for (int n = 0; ok; ++n) {
-      int w;
-      if (!next_item(n, w)) { ok = false; break; }
-      if (w >= n_items) break;
       int n_it, diag_i;
       bool key_live;
       {
         BwdItem it;
-        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        const int got = get_item(n, it);
+        if (got < 0) { ok = false; break; }
+        if (got == 1) break;
+        if (got == 2) continue;
         n_it = it.n_it;
         diag_i = causal ? it.kb - it.i_begin : -1;  // iteration of the diagonal tile
         key_live = it.kb * C::BK + r < it.sv.len;
@@ -872,8 +999,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
         }
         tc_fence_after();
-        BwdItem it;  // decoded again: keeps the tile loop's registers free
-        bwd_item<C::BK, C::BQ>(a, list, w, it);
+        BwdItem it;  // read again: keeps the tile loop's registers free
+        reload_item(n, it);
         const int k0 = it.kb * C::BK;
         const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
         if (it.tail_unit >= 0) {
@@ -948,6 +1075,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       }
       ++ui;
       g0 += n_it;
+      release_item(n);
     }
     if (!ok) *abort_flag = 1;
     if (lane == 0) bulk_wait_group_all();  // the epilogue's tensor stores have completed
@@ -962,14 +1090,14 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     int ui = 0, g0 = 0;  // items and query tiles before this item
     bool ok = true;
     for (int n = 0; ok; ++n) {
-      int w;
-      if (!next_item(n, w)) { ok = false; break; }
-      if (w >= n_items) break;
       size_t row_first;  // workspace row of the item's first query tile
       int n_it;
       {
         BwdItem it;
-        if (!bwd_item<C::BK, C::BQ>(a, list, w, it)) continue;
+        const int got = get_item(n, it);
+        if (got < 0) { ok = false; break; }
+        if (got == 1) break;
+        if (got == 2) continue;
         row_first = (size_t)it.sv.plane * a.ws_rows + (size_t)it.sv.start + (size_t)it.i_begin * C::BQ;
         n_it = it.n_it;
       }
@@ -1051,8 +1179,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         if (!__all_sync(0xffffffffu, w_ok)) { *abort_flag = 1; ok = false; break; }
       }
       tc_fence_after();
-      BwdItem it;  // decoded again: keeps the tile loop's registers free
-      bwd_item<C::BK, C::BQ>(a, list, w, it);
+      BwdItem it;  // read again: keeps the tile loop's registers free
+      reload_item(n, it);
       const int r = wq * 32 + lane;
       const int k0 = it.kb * C::BK;
       if (it.tail_unit >= 0) {
@@ -1143,6 +1271,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       }
       ++ui;
       g0 += n_it;
+      release_item(n);
     }
     // every bulk reduction must have read its staging block before the CTA
     // exits; the additions land before the kernel ends
@@ -1165,13 +1294,13 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
     constexpr int RPW = 32 / (D / 8);
     const long long rows = (long long)a.planes * a.ws_rows;
     const long long warps = (rows + RPW - 1) / RPW;
-    const long long blocks = (warps * 32 + 255) / 256;
+    const long long blocks = (warps * 32 + 255) / 256 + (a.nseq > 0 ? 1 : 0);  // + the schedule block
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (stages & kStageMain) {
-    const bool dyn = a.items > 0 && a.seq.causal;
+    const bool dyn = a.items > 0 && (a.seq.causal || a.seq.cu_seqlens != nullptr);
     e = cudaFuncSetAttribute(dyn ? bwd_main_kernel<D, true> : bwd_main_kernel<D, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -1180,8 +1309,11 @@ cudaError_t launch_bwd_d(const BwdArgs& a, int BH, unsigned stages, cudaStream_t
     if (a.items > 0) {
       // persistent grid over the item list: one CTA per SM (each holds all of
       // TMEM and most of shared memory)
-      if (a.seq.cu_seqlens || a.item_counter == nullptr) return cudaErrorInvalidValue;
-      if (a.seq.causal) {
+      if (a.item_counter == nullptr) return cudaErrorInvalidValue;
+      if (a.seq.cu_seqlens) {
+        if (a.nseq < 1 || a.splits != 1 || (long long)a.items != (long long)BH * kblocks)
+          return cudaErrorInvalidValue;
+      } else if (a.seq.causal) {
         const int hpg = causal_heads_per_group(BH, 8ll * a.seq.N * D, 48ll << 20);
         if (a.splits != 1 || a.causal_hpg != hpg ||
             (long long)a.items != (long long)hpg * kblocks * ((BH + hpg - 1) / hpg))

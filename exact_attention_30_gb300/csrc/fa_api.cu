@@ -184,7 +184,9 @@ BwdWorkspaceLayout bwd_layout(const SeqArgs& sq, int B, int d, fa_dtype dt) {
   if (!sq.causal && sq.cu_seqlens == nullptr)
     L.plan = plan_bwd_tail((long long)B * sq.H * ((sq.N + 127) / 128), (sq.N + 127) / 128, fwd_slots());
   L.sched = L.part + bwd_tail_part_bytes(L.plan, d);
-  L.total = L.sched + 256;
+  // the main kernel's schedule: item counter, item total and, for a packed
+  // batch, the sequence order and the B + 1 unit prefix sums
+  L.total = L.sched + align_up(sizeof(int) * (2 + (sq.cu_seqlens ? 2 * (size_t)B + 1 : 0)), 256);
   return L;
 }
 
@@ -386,7 +388,15 @@ fa_status bwd_impl(unsigned stages, const void* Q, const void* K, const void* V,
   a.splits = L.plan.splits;
   a.dKVpart = L.plan.splits > 1 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
   a.item_counter = reinterpret_cast<int*>(ws + L.sched);
-  if (sq.cu_seqlens == nullptr) {
+  if (sq.cu_seqlens != nullptr) {
+    // packed batch: every (sequence, head, key tile) unit, at most
+    // B * H * ceil(max_seqlen / 128); the preprocess writes the exact total
+    const long long bound = (long long)BH * ((sq.N + 127) / 128);
+    if (bound <= (1ll << 30)) {  // else one CTA per unit of the 2-D grid
+      a.nseq = B;
+      a.items = (int)bound;
+    }
+  } else {
     // fixed length: the persistent grid's item list
     const int kblocks = (sq.N + 127) / 128;
     if (sq.causal) {

@@ -129,11 +129,14 @@ struct BwdArgs {
   // n_full + n_tail * splits, taken by min(items, SM count) CTAs with stride
   // gridDim.x; causal causal_hpg * key tiles * head groups (heads past BH
   // skipped), the first by block index, the rest from *item_counter (zeroed
-  // by the preprocess stage). 0: one unit per CTA of the 2-D grid (packed
-  // batches).
+  // by the preprocess stage); packed batches (an upper bound here; the total
+  // is in the schedule the preprocess writes) sequences longest first, then
+  // heads, then key tiles, from the counter as well. 0: one unit per CTA of
+  // the 2-D/3-D grids.
   int items;
   int causal_hpg;     // heads per group of the causal item order
-  int* item_counter;  // in the workspace
+  int* item_counter;  // in the workspace: the schedule ints (counter first)
+  int nseq;           // packed batches: sequences (their schedule follows the counter); else 0
 };
 cudaError_t launch_bwd_bf16(const BwdArgs& a, int BH, int d, unsigned stages, cudaStream_t st);
 // The backward's tail split for `units` (batch*head, key tile) units with n_q

@@ -17,9 +17,9 @@ import pytest
 import torch
 
 import exact_attention_30_gb300 as fa
-from exact_attention_30_gb300.inputs import random_qkv
-from oracle import attention_bwd
-from parity_utils import grad_within, rel_max, to64
+from exact_attention_30_gb300.inputs import random_qkv, random_varlen
+from oracle import attention_bwd, varlen_attention_bwd
+from parity_utils import TOL_BF16_GRAD, grad_within, rel_max, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -71,3 +71,37 @@ def test_persistent_backward_repeats_dk_dv_bit_for_bit():
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
     # dQ is added by the TMA engine in whatever order the items arrive
     assert (g1[0].float() - g2[0].float()).abs().max() <= 1e-2 * g1[0].float().abs().max()
+
+
+def _varlen_case(lens, H, d, causal, seed):
+    q, k, v, do, cu = random_varlen(lens, H, d, torch.bfloat16, seed=seed)
+    scale = 1 / math.sqrt(d)
+    args = [t.cuda() for t in (q, k, v)]
+    cuc = cu.cuda()
+    o, lse = fa.fa_fwd_varlen(*args, cuc, max(lens), scale, causal=causal)
+    grads = fa.fa_bwd_varlen(*args, o, do.cuda(), lse, cuc, max(lens), scale, causal=causal)
+    torch.cuda.synchronize()
+    assert fa.fa_check_device_status() == fa.FA_OK
+    ref = varlen_attention_bwd(to64(q), to64(k), to64(v), to64(do), cu.tolist(), scale, causal)
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, ref):
+        assert rel_max(g, r) <= TOL_BF16_GRAD, (name, rel_max(g, r))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_backward_packed_batch_many_sequences(d, causal):
+    """A packed batch of 40 sequences (empty ones among them) whose units
+    outnumber the SMs: the preprocess ranks the sequences by length and the
+    CTAs take the units, longest sequence first, from the device counter."""
+    rng = np.random.default_rng(40 + d)
+    lens = [int(x) for x in rng.integers(0, 700, size=40)]
+    lens[3] = lens[17] = 0
+    _varlen_case(lens, 4, d, causal, seed=d + int(causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_backward_packed_batch_past_1024_sequences(causal):
+    """More than 1024 sequences: the schedule keeps their index order."""
+    rng = np.random.default_rng(1100)
+    lens = [int(x) for x in rng.integers(1, 48, size=1100)]
+    _varlen_case(lens, 1, 64, causal, seed=7 + int(causal))
