@@ -396,8 +396,7 @@ __device__ __noinline__ bool bwd_item(const BwdArgs& a, bool list, int w, BwdIte
 // free.
 // The set-up, the TMEM allocation and the CTA turnaround are paid once per SM,
 // and the next item's first loads and products overlap this item's last
-// tile and epilogue. The producer takes each item and publishes it to the
-// other roles through a small ring in shared memory; the rings and the
+// tile and epilogue. The rings and the
 // per-tile barriers continue across items (global tile index g), the K/V
 // tile and the dV/dK accumulators are handed over per item (kv_empty; the
 // next item's first dV and dK products come after the epilogue: acc_empty
@@ -411,7 +410,7 @@ template <int D, bool DYN>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdArgs a) {
   using C = BwdCfg<D>;
   // Who writes an item's dV and dK: the dQ warps (the softmax warps go
-  // straight on to the next item), except in the causal-list kernel at
+  // straight on to the next item), except in the counter kernel (DYN) at
   // d = 128, where the softmax warps do (there the dQ warps' register budget
   // spills). Measured both ways; each is the faster one where it is used.
   constexpr bool EPI_DQ = (D == 64) || !DYN;
