@@ -67,6 +67,8 @@ _SIGNATURES = {
     "fa_debug_fwd_skip_load": (_ci, [_vp] * 5 + [_ci, _ci, _ci, _ci, _cf, _ci, ctypes.c_longlong, _vp]),
     "fa_debug_bwd_skip_load": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci,
                                                   ctypes.c_longlong, _vp]),
+    "fa_debug_bwd_skip_load_ex": (_ci, [_vp] * 10 + [_sz, _ci, _ci, _ci, _ci, _cf, _ci, _ci,
+                                                     ctypes.c_longlong, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_ci]),
     "fa_version": (_ci, []),
 }

@@ -706,6 +706,21 @@ fa_status fa_debug_bwd_skip_load(const void* Q, const void* K, const void* V, co
                   clamp_limit(limit_ns));
 }
 
+fa_status fa_debug_bwd_skip_load_ex(const void* Q, const void* K, const void* V, const void* O,
+                                    const void* dO, const float* LSE, void* dQ, void* dK,
+                                    void* dV, void* workspace, size_t workspace_bytes, int B,
+                                    int H, int N, int d, float scale, int flags, int skip_tile,
+                                    long long limit_ns, void* stream) {
+  if (flags & ~FA_CAUSAL) return FA_ERR_INVALID_ARG;
+  const fa_status s = check_shape(B, H, N, d, scale, FA_BF16);
+  if (s != FA_OK) return s;
+  if (skip_tile < 1 || skip_tile >= (N + bwd_query_tile(d) - 1) / bwd_query_tile(d))
+    return FA_ERR_INVALID_ARG;
+  return bwd_impl(kStageAll, Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes,
+                  fixed_seq(H, N, d, (flags & FA_CAUSAL) != 0), B, d, scale, FA_BF16, stream,
+                  skip_tile, clamp_limit(limit_ns));
+}
+
 fa_status fa_debug_timeout_probe(long long limit_ns, void* stream) {
   int* status = device_status_ptr();
   if (!status) return FA_ERR_CUDA;

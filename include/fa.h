@@ -378,6 +378,19 @@ fa_status fa_debug_bwd_skip_load(const void* Q, const void* K, const void* V, co
                                  void* workspace, size_t workspace_bytes, int B, int H, int N,
                                  int d, float scale, int skip_tile, long long limit_ns,
                                  void* stream);
+/*
+ * fa_debug_bwd_skip_load with flags: FA_CAUSAL runs the causal backward,
+ * whose persistent CTAs take their units from the device counter and pass
+ * them on through the shared-memory item ring (the ring's bounded waits then
+ * run out too). The workspace must hold fa_bwd_workspace_bytes for the
+ * problem. Errors: as fa_debug_bwd_skip_load, plus FA_ERR_INVALID_ARG for
+ * flags other than 0 and FA_CAUSAL.
+ */
+fa_status fa_debug_bwd_skip_load_ex(const void* Q, const void* K, const void* V, const void* O,
+                                    const void* dO, const float* LSE, void* dQ, void* dK,
+                                    void* dV, void* workspace, size_t workspace_bytes, int B,
+                                    int H, int N, int d, float scale, int flags, int skip_tile,
+                                    long long limit_ns, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* fa_status_string(fa_status s);

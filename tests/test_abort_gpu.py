@@ -98,3 +98,40 @@ def test_skip_hooks_reject_tiles_outside_the_problem():
         assert lib.fa_debug_bwd_skip_load(*([fake] * 10), 1 << 30, 1, 1, 1024, 128,
                                           ctypes.c_float(0.1), bad, LIMIT_NS,
                                           None) == fa.FA_ERR_INVALID_ARG
+        assert lib.fa_debug_bwd_skip_load_ex(*([fake] * 10), 1 << 30, 1, 1, 1024, 128,
+                                             ctypes.c_float(0.1), fa.FA_CAUSAL, bad, LIMIT_NS,
+                                             None) == fa.FA_ERR_INVALID_ARG
+    # flags other than FA_CAUSAL
+    assert lib.fa_debug_bwd_skip_load_ex(*([fake] * 10), 1 << 30, 1, 1, 1024, 128, ctypes.c_float(0.1),
+                                         2, 1, LIMIT_NS, None) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_backward_skipped_query_tile_times_out_then_recovers(d):
+    """The causal backward: persistent CTAs taking units from the device
+    counter and passing them on through the item ring. Every CTA skips the
+    third tile of its walk; the bounded waits (tile and ring) run out, the
+    timeout is reported, and a normal causal call afterwards matches the
+    oracle."""
+    lib = fa.load_library()
+    B, H, N = 1, 24, 768
+    q, k, v, do = (t.cuda() for t in random_qkv(B, H, N, d, torch.bfloat16, seed=61 + d))
+    scale = 1 / math.sqrt(d)
+    stream = torch.cuda.current_stream().cuda_stream
+    o, lse = fa.fa_fwd(q, k, v, scale, causal=True)
+    assert fa.fa_check_device_status() == fa.FA_OK
+    ws_bytes = fa.fa_bwd_workspace_bytes(B, H, N, d)  # covers the causal layout (no split partials)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    rc = lib.fa_debug_bwd_skip_load_ex(*_ptrs(q, k, v, o, do, lse, dq, dk, dv, ws), ws_bytes, B, H, N,
+                                       d, ctypes.c_float(scale), fa.FA_CAUSAL, 2, LIMIT_NS, stream)
+    assert rc == fa.FA_OK
+    assert fa.fa_check_device_status() == fa.FA_ERR_TIMEOUT
+    assert fa.fa_check_device_status() == fa.FA_OK
+    grads = fa.fa_bwd(q, k, v, o, do, lse, scale, causal=True)
+    assert fa.fa_check_device_status() == fa.FA_OK
+    q64, k64, v64, do64 = to64(q), to64(k), to64(v), to64(do)
+    for h in (0, H - 1):
+        ref = attention_bwd(q64[0, h], k64[0, h], v64[0, h], do64[0, h], scale, causal=True)
+        for g, r in zip(grads, ref):
+            assert rel_max(g[0, h], r) <= TOL_BF16_GRAD
