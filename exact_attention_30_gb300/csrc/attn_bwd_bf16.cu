@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       for (int n = 0; ok; ++n) {
         // the item, past any with nothing to do (heads padding the last
         // causal head group)
-        BwdItem it;
+        BwdItem it{};
         bool end = false;
         for (;;) {
           if (w >= n_items) { end = true; break; }
