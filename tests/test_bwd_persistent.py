@@ -100,8 +100,17 @@ def test_persistent_backward_packed_batch_many_sequences(d, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_persistent_backward_packed_batch_past_1024_sequences(causal):
+@pytest.mark.parametrize("d", [64, 128])
+def test_persistent_backward_packed_batch_past_1024_sequences(d, causal):
     """More than 1024 sequences: the schedule keeps their index order."""
     rng = np.random.default_rng(1100)
     lens = [int(x) for x in rng.integers(1, 48, size=1100)]
-    _varlen_case(lens, 1, 64, causal, seed=7 + int(causal))
+    _varlen_case(lens, 1, d, causal, seed=7 + d + int(causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_backward_packed_batch_long_sequences(causal):
+    """Six sequences of 1500-4100 keys (12 to 33 key tiles), 12 heads: long
+    units, the longest sequences' units first."""
+    lens = [1500, 4100, 2049, 3333, 1999, 2600]
+    _varlen_case(lens, 12, 128, causal, seed=99 + int(causal))
