@@ -47,6 +47,18 @@ def test_workspace_size_is_host_only(lib):
     assert lib.fa_bwd_workspace_bytes(1, 1, 1000, 64, fa.FA_F32) >= 4000
 
 
+def test_packed_batch_workspace_holds_the_schedule(lib):
+    # the main kernel's schedule follows the per-row buffers: the unit counter
+    # and total, then the sequence order and the B + 1 unit prefix sums
+    H, total, max_len, d = 2, 4096, 2048, 64
+    one = lib.fa_bwd_varlen_workspace_bytes(2, H, total, max_len, d, fa.FA_BF16)
+    many = lib.fa_bwd_varlen_workspace_bytes(2000, H, total, max_len, d, fa.FA_BF16)
+    assert one > 0 and one % 256 == 0 and many % 256 == 0
+    assert many - one >= 4 * 2 * (2000 - 2)  # two ints more per sequence
+    # fixed length: the counter and the total only (one 256-byte block)
+    assert fa.fa_bwd_workspace_bytes(1, 1, 128, 64) >= 128 * 64 * 4 + 2 * 128 * 4 + 256
+
+
 FAKE = 0x10000  # an aligned non-null value: never dereferenced, validation fails first
 
 
